@@ -1,0 +1,205 @@
+"""Pins for the CPU oracle: checks that tie it to something other than itself.
+
+Each ``check_*`` function takes an ``oracle.Oracle`` instance and raises
+AssertionError when the oracle disagrees with an independent fact:
+
+* exact rational brute force on tiny shapes (Python ``fractions``),
+* identity matrices (A.I = A and I.B = B, rectangular too),
+* closed-form products of structured matrices,
+* integer-valued inputs against exact int64 arithmetic,
+* a float64 library matmul,
+* strided (padded) operands against compact ones,
+* sampled rows/columns against the full product,
+* the transpose identity (A.B)^T = B^T.A^T,
+* the absolute-sum S against the product of |A| and |B|,
+* IEEE propagation of NaN, the empty sum (K = 0), rejected arguments.
+
+The definition being pinned is C_ij = sum_k A_ik B_kj ("Перемножение матриц:
+наивное и тайловое", section 1), with row-major storage at row*ld + col.
+``tests/test_oracle.py`` runs every check on the real oracle;
+``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
+oracle's C source and requires each to fail at least one check.
+"""
+
+from __future__ import annotations
+
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import workloads
+
+
+def _rand(rows, cols, dist, seed):
+    A, _ = workloads.make_operands(rows, 1, cols, dist, seed)
+    return A.numpy()
+
+
+def _pair(M, N, K, dist, seed):
+    A, B = workloads.make_operands(M, N, K, dist, seed)
+    return A.numpy(), B.numpy()
+
+
+def check_bruteforce_rational(o, max_dim=5, seed=11):
+    """All M, N, K in 1..max_dim: exact rational sum of exact products."""
+    rng = np.random.default_rng(seed)
+    for M, N, K in itertools.product(range(1, max_dim + 1), repeat=3):
+        # Mix magnitudes so that the double sum actually rounds.
+        A = (rng.standard_normal((M, K)) * 2.0 ** rng.integers(-20, 20, (M, K))).astype(np.float32)
+        B = (rng.standard_normal((K, N)) * 2.0 ** rng.integers(-20, 20, (K, N))).astype(np.float32)
+        C, S = o.sgemm(M, N, K, A, K, B, N)
+        for i in range(M):
+            for j in range(N):
+                exact = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j]))
+                            for k in range(K))
+                sabs = sum(abs(Fraction(float(A[i, k])) * Fraction(float(B[k, j])))
+                           for k in range(K))
+                bound = Fraction(K, 2 ** 53) * sabs
+                err = abs(Fraction(float(C[i, j])) - exact)
+                assert err <= bound, (M, N, K, i, j, float(err), float(bound))
+                assert Fraction(float(S[i, j])) >= sabs * (1 - Fraction(K, 2 ** 52)), (M, N, K, i, j)
+                assert abs(Fraction(float(S[i, j])) - sabs) <= bound, (M, N, K, i, j)
+
+
+def check_identity(o):
+    """A.I = A and I.B = B exactly, with square and rectangular identities."""
+    for (M, K, N) in [(5, 7, 7), (7, 5, 3), (3, 4, 9), (33, 17, 17), (1, 1, 1)]:
+        A = _rand(M, K, "normal", 1)
+        I = workloads.special_matrix("identity", K, N).numpy()
+        C, _ = o.sgemm(M, N, K, A, K, I, N)
+        want = np.zeros((M, N))
+        w = min(K, N)
+        want[:, :w] = A[:, :w].astype(np.float64)
+        assert np.array_equal(C, want), (M, K, N)
+        I2 = workloads.special_matrix("identity", M, K).numpy()
+        B = _rand(K, N, "normal", 2)
+        C2, _ = o.sgemm(M, N, K, I2, K, B, N)
+        want2 = np.zeros((M, N))
+        h = min(M, K)
+        want2[:h, :] = B[:h, :].astype(np.float64)
+        assert np.array_equal(C2, want2), (M, K, N)
+
+
+def check_closed_forms(o):
+    """Structured products with closed forms (all exact in double)."""
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (16, 9, 33), (40, 17, 129)]:
+        sm = workloads.special_matrix
+        i = np.arange(M, dtype=np.float64).reshape(M, 1)
+        j = np.arange(N, dtype=np.float64).reshape(1, N)
+        # all ones: every entry is K
+        C, _ = o.sgemm(M, N, K, sm("ones", M, K).numpy(), K, sm("ones", K, N).numpy(), N)
+        assert np.array_equal(C, np.full((M, N), float(K))), ("ones", M, N, K)
+        # A_ik = 1, B_kj = k: sum_k k = K(K-1)/2
+        C, _ = o.sgemm(M, N, K, sm("ones", M, K).numpy(), K, sm("row_index", K, N).numpy(), N)
+        assert np.array_equal(C, np.full((M, N), K * (K - 1) / 2)), ("sum k", M, N, K)
+        # A_ik = i, B_kj = j: C_ij = i * j * K
+        C, _ = o.sgemm(M, N, K, sm("row_index", M, K).numpy(), K, sm("col_index", K, N).numpy(), N)
+        assert np.array_equal(C, i * j * K), ("i*j*K", M, N, K)
+        # A_ik = i, B_kj = k: C_ij = i * K(K-1)/2   (a transposed A would differ)
+        C, _ = o.sgemm(M, N, K, sm("row_index", M, K).numpy(), K, sm("row_index", K, N).numpy(), N)
+        assert np.array_equal(C, np.broadcast_to(i * (K * (K - 1) / 2), (M, N))), ("i*sum k", M, N, K)
+        # A_ik = k + 1, B_kj = k + 1: sum of squares K(K+1)(2K+1)/6
+        C, _ = o.sgemm(M, N, K, sm("col_plus1", M, K).numpy(), K, sm("row_plus1", K, N).numpy(), N)
+        assert np.array_equal(C, np.full((M, N), K * (K + 1) * (2 * K + 1) / 6)), ("squares", M, N, K)
+        # A_ik = (-1)^k, B = ones: K mod 2 (signs must cancel)
+        C, S = o.sgemm(M, N, K, sm("alt_sign_col", M, K).numpy(), K, sm("ones", K, N).numpy(), N)
+        assert np.array_equal(C, np.full((M, N), float(K % 2))), ("alt", M, N, K)
+        assert np.array_equal(S, np.full((M, N), float(K))), ("alt abs", M, N, K)
+        # A_ik = 1, B_kj = j: C_ij = K * j   (B must be read along its row)
+        C, _ = o.sgemm(M, N, K, sm("ones", M, K).numpy(), K, sm("col_index", K, N).numpy(), N)
+        assert np.array_equal(C, np.broadcast_to(K * j, (M, N))), ("K*j", M, N, K)
+
+
+def check_integer_exact(o):
+    """Integer inputs in [-4, 4]: equal to exact int64 matrix products."""
+    for n, (M, N, K) in enumerate([(1, 1, 1), (7, 13, 5), (64, 48, 100), (31, 33, 257)]):
+        A, B = _pair(M, N, K, "int", 100 + n)
+        C, S = o.sgemm(M, N, K, A, K, B, N)
+        Ai, Bi = A.astype(np.int64), B.astype(np.int64)
+        assert np.array_equal(C, (Ai @ Bi).astype(np.float64)), (M, N, K)
+        assert np.array_equal(S, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64)), (M, N, K)
+
+
+def check_float64_library(o):
+    """Random normal inputs: within 1e-12 * S of torch's float64 matmul."""
+    for n, (M, N, K) in enumerate([(64, 64, 64), (100, 37, 300), (257, 129, 511)]):
+        A, B = _pair(M, N, K, "normal", 200 + n)
+        C, S = o.sgemm(M, N, K, A, K, B, N)
+        ref = (torch.from_numpy(A).double() @ torch.from_numpy(B).double()).numpy()
+        assert np.all(np.abs(C - ref) <= 1e-12 * S), (M, N, K)
+
+
+def check_strides(o):
+    """Padded leading dimensions give the compact result; padding is never read."""
+    M, N, K = 19, 23, 29
+    A, B = workloads.make_operands(M, N, K, "uniform", 7)
+    Ap, Bp = workloads.make_operands(M, N, K, "uniform", 7, lda=K + 5, ldb=N + 3)
+    C, S = o.sgemm(M, N, K, A.numpy(), K, B.numpy(), N)
+    Cp, Sp = o.sgemm(M, N, K, Ap.numpy(), K + 5, Bp.numpy(), N + 3)
+    assert not np.isnan(Cp).any()
+    assert np.array_equal(C, Cp) and np.array_equal(S, Sp)
+
+
+def check_sampled(o):
+    """Sampled rows and columns equal the same rows/columns of the full product."""
+    M, N, K = 37, 41, 53
+    A, B = _pair(M, N, K, "normal", 9)
+    C, S = o.sgemm(M, N, K, A, K, B, N)
+    rows = workloads.sample_indices(M, 9, 1)
+    cols = workloads.sample_indices(N, 9, 2)
+    Cr, Sr = o.sgemm_rows(M, N, K, A, K, B, N, rows)
+    Cc, Sc = o.sgemm_cols(M, N, K, A, K, B, N, cols)
+    assert np.array_equal(Cr, C[rows]) and np.array_equal(Sr, S[rows])
+    assert np.array_equal(Cc, C[:, cols]) and np.array_equal(Sc, S[:, cols])
+
+
+def check_transpose(o):
+    """(A.B)^T = B^T.A^T, element for element (same k order)."""
+    M, N, K = 21, 14, 33
+    A, B = _pair(M, N, K, "normal", 5)
+    C, _ = o.sgemm(M, N, K, A, K, B, N)
+    Bt = np.ascontiguousarray(B.T)
+    At = np.ascontiguousarray(A.T)
+    Ct, _ = o.sgemm(N, M, K, Bt, K, At, M)
+    assert np.array_equal(C, Ct.T)
+
+
+def check_abs_sum(o):
+    """S(A, B) equals the product of |A| and |B|, and bounds |C|."""
+    M, N, K = 17, 19, 65
+    A, B = _pair(M, N, K, "normal", 6)
+    C, S = o.sgemm(M, N, K, A, K, B, N)
+    Cabs, _ = o.sgemm(M, N, K, np.abs(A), K, np.abs(B), N)
+    assert np.array_equal(S, Cabs)
+    assert np.all(np.abs(C) <= S)
+
+
+def check_special_values(o):
+    """NaN in row i of A makes row i of C NaN and nothing else; K=0 is zero."""
+    M, N, K = 6, 5, 4
+    A, B = _pair(M, N, K, "uniform", 3)
+    A = A.copy()
+    A[2, 1] = np.nan
+    C, _ = o.sgemm(M, N, K, A, K, B, N)
+    assert np.isnan(C[2]).all()
+    assert not np.isnan(np.delete(C, 2, axis=0)).any()
+    C0, S0 = o.sgemm(3, 4, 0, np.zeros(1, np.float32), 1, np.zeros(1, np.float32), 4)
+    assert np.array_equal(C0, np.zeros((3, 4))) and np.array_equal(S0, np.zeros((3, 4)))
+    Ce, _ = o.sgemm(0, 4, 3, np.zeros(1, np.float32), 3, np.zeros(12, np.float32), 4)
+    assert Ce.shape == (0, 4)
+
+
+ALL_CHECKS = [
+    check_bruteforce_rational,
+    check_identity,
+    check_closed_forms,
+    check_integer_exact,
+    check_float64_library,
+    check_strides,
+    check_sampled,
+    check_transpose,
+    check_abs_sum,
+    check_special_values,
+]
