@@ -1,0 +1,119 @@
+"""GB300 (sm_103a) single-precision GEMM: C = A . B on row-major FP32 matrices.
+
+This package is a thin ctypes binding over the C ABI in ``include/sgemm.h``
+(``_build/libsgemm.so``, compiled from ``csrc/`` by ``build.py``). Its
+functions carry the same names and arguments as the C functions and only
+marshal arguments: pointers are plain integers (device addresses, e.g. a
+torch tensor's ``data_ptr()``), streams are integers (``cudaStream_t``,
+e.g. ``torch.cuda.current_stream().cuda_stream``; 0 is the default stream).
+Every step of the product runs in the library's CUDA kernels; there is no
+CPU fallback, and loading fails loudly if the library cannot be built or
+loaded.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_VALUE = 1
+SGEMM_ERR_OVERFLOW = 2
+SGEMM_ERR_ALLOC = 3
+SGEMM_ERR_LAUNCH = 4
+SGEMM_ERR_TIMEOUT = 5
+SGEMM_ERR_CUDA = 6
+SGEMM_ERR_UNSUPPORTED = 7
+
+# Every function declared in include/sgemm.h.
+EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
+            "sgemm_num_configs", "sgemm_config_name", "sgemm_plan")
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {sgemm_error_string(code)} ({code})")
+        self.code = code
+
+
+def load(rebuild: bool = False):
+    """Build (if needed) and load the library; raises if either fails."""
+    global _lib
+    with _lock:
+        if _lib is None or rebuild:
+            path = _build.build(force=rebuild)
+            lib = ctypes.CDLL(path)
+            lib.sgemm.restype = ctypes.c_int
+            lib.sgemm.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+            lib.sgemm_ex.restype = ctypes.c_int
+            lib.sgemm_ex.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                     ctypes.c_int, _vp]
+            lib.sgemm_check_status.restype = ctypes.c_int
+            lib.sgemm_check_status.argtypes = [_vp]
+            lib.sgemm_error_string.restype = ctypes.c_char_p
+            lib.sgemm_error_string.argtypes = [ctypes.c_int]
+            lib.sgemm_num_configs.restype = ctypes.c_int
+            lib.sgemm_num_configs.argtypes = []
+            lib.sgemm_config_name.restype = ctypes.c_char_p
+            lib.sgemm_config_name.argtypes = [ctypes.c_int]
+            lib.sgemm_plan.restype = ctypes.c_int
+            lib.sgemm_plan.argtypes = [_i64, _i64, _i64, _i64, _i64, _i64,
+                                       ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                       ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_int)]
+            _lib = lib
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def sgemm(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C = A . B on device pointers; returns the status code (0 = OK)."""
+    return load().sgemm(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, config, stream=0) -> int:
+    """sgemm() with a forced kernel configuration (-1 = automatic)."""
+    return load().sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, config, stream)
+
+
+def sgemm_check_status(stream=0) -> int:
+    """Waits for `stream`, reads and clears the device error word."""
+    return load().sgemm_check_status(stream)
+
+
+def sgemm_error_string(code: int) -> str:
+    return load().sgemm_error_string(code).decode()
+
+
+def sgemm_num_configs() -> int:
+    return load().sgemm_num_configs()
+
+
+def sgemm_config_name(config: int) -> str:
+    return load().sgemm_config_name(config).decode()
+
+
+def sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms):
+    """Host-only: (status, config, pack_a, pack_b) that sgemm() would use."""
+    cfg, pa, pb = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    rc = load().sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms,
+                           ctypes.byref(cfg), ctypes.byref(pa), ctypes.byref(pb))
+    return rc, cfg.value, pa.value, pb.value
+
+
+def config_ids() -> dict:
+    """Map of configuration name -> id."""
+    return {sgemm_config_name(i): i for i in range(sgemm_num_configs())}

@@ -1,0 +1,127 @@
+// General-purpose kernels: the predicated shared-memory tiled product (any
+// shape, stride and alignment), the zero fill used when K == 0, and the
+// operand pack that gives misaligned operands 16-byte-aligned rows.
+#include "common.cuh"
+
+namespace sgemm_gb300 {
+
+// ---------------------------------------------------------------------------
+// Shared-memory tiled product, one thread per element of C.
+//
+// Chapter 9: Optimised Matrix Multiplication, section 9.4 (shared-memory
+// tiling): a T x T block of threads computes a T x T tile of C, marching K in
+// steps of T; each step stages a T x T tile of A and of B in shared memory,
+// padded by one column so the column walk is free of bank conflicts, behind
+// a barrier before the tile is read and another before it is overwritten
+// ("Перемножение матриц: наивное и тайловое", section 2, on why both
+// barriers are needed). Unlike the pages' listing, every global access is
+// predicated, so M, N, K need not be multiples of T and any leading dimension
+// and alignment is accepted; out-of-range tile entries are zero.
+// ---------------------------------------------------------------------------
+template <int T>
+__global__ void __launch_bounds__(T * T)
+sgemm_tiled_simple_kernel(int64_t M, int64_t N, int64_t K,
+                          const float *__restrict__ A, int64_t lda,
+                          const float *__restrict__ B, int64_t ldb,
+                          float *__restrict__ C, int64_t ldc)
+{
+    __shared__ float sA[T][T + 1];
+    __shared__ float sB[T][T + 1];
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int64_t tiles_n = (N + T - 1) / T;
+    const int64_t tiles = ((M + T - 1) / T) * tiles_n;
+
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t row = (t / tiles_n) * T + ty;
+        const int64_t col = (t % tiles_n) * T + tx;
+        float acc = 0.0f;
+        for (int64_t k0 = 0; k0 < K; k0 += T) {
+            sA[ty][tx] = (row < M && k0 + tx < K) ? A[row * lda + k0 + tx] : 0.0f;
+            sB[ty][tx] = (k0 + ty < K && col < N) ? B[(k0 + ty) * ldb + col] : 0.0f;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < T; ++k) acc = fmaf(sA[ty][k], sB[k][tx], acc);
+            __syncthreads();
+        }
+        if (row < M && col < N) C[row * ldc + col] = acc;
+    }
+}
+
+cudaError_t launch_tiled_simple(const GemmArgs &g, cudaStream_t stream)
+{
+    constexpr int T = 16;
+    const int64_t tiles = ((g.M + T - 1) / T) * ((g.N + T - 1) / T);
+    const int64_t cap = (int64_t)g.num_sms * 64;
+    const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+    sgemm_tiled_simple_kernel<T><<<grid, dim3(T, T), 0, stream>>>(
+        g.M, g.N, g.K, g.A, g.lda, g.B, g.ldb, g.C, g.ldc);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Zero fill of an M x N block of C (the empty sum, K == 0).
+// ---------------------------------------------------------------------------
+__global__ void zero_fill_kernel(float *__restrict__ C, int64_t M, int64_t N,
+                                 int64_t ldc)
+{
+    const int64_t total = M * N;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / N, j = e % N;
+        C[i * ldc + j] = 0.0f;
+    }
+}
+
+cudaError_t launch_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc,
+                             cudaStream_t stream)
+{
+    const int64_t total = M * N;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    zero_fill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Pack: dst[r * ld_dst + c] = src[r * ld_src + c] for r < rows, c < cols.
+// Each warp copies one row segment per iteration, so both the 4-byte reads
+// (of a possibly misaligned source) and the writes are coalesced. Entries of
+// dst beyond `cols` are left as they are: the product never reads them (its
+// tensor maps describe only `cols` columns and fill the rest with zero).
+// ---------------------------------------------------------------------------
+__global__ void pack_kernel(const float *__restrict__ src, int64_t rows,
+                            int64_t cols, int64_t ld_src,
+                            float *__restrict__ dst, int64_t ld_dst)
+{
+    const int64_t segs = (cols + 255) / 256;       // 256-column segments per row
+    const int64_t work = rows * segs;
+    const int warps = blockDim.x / 32;
+    const int lane = threadIdx.x & 31;
+    for (int64_t w = blockIdx.x * (int64_t)warps + threadIdx.x / 32; w < work;
+         w += (int64_t)gridDim.x * warps) {
+        const int64_t r = w / segs;
+        const int64_t c0 = (w % segs) * 256;
+        const float *s = src + r * ld_src;
+        float *d = dst + r * ld_dst;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t c = c0 + q * 32 + lane;
+            if (c < cols) d[c] = s[c];
+        }
+    }
+}
+
+cudaError_t launch_pack(const float *src, int64_t rows, int64_t cols,
+                        int64_t ld_src, float *dst, int64_t ld_dst,
+                        cudaStream_t stream)
+{
+    const int64_t work = rows * ((cols + 255) / 256);
+    int64_t blocks = (work + 7) / 8;
+    if (blocks > 8192) blocks = 8192;
+    if (blocks < 1) blocks = 1;
+    pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, rows, cols, ld_src,
+                                                     dst, ld_dst);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm_gb300

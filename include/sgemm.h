@@ -1,0 +1,152 @@
+/*
+ * sgemm.h — C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation (one call computes it for one problem):
+ *
+ *     C[i*ldc + j] = sum_{k=0}^{K-1} A[i*lda + k] * B[k*ldb + j]
+ *                    for 0 <= i < M, 0 <= j < N
+ *
+ * Definition: "Перемножение матриц: наивное и тайловое" (Matrix
+ * multiplication: naive and tiled), section 1 — element C_row,col is the dot
+ * product of row `row` of A and column `col` of B; matrices are stored row by
+ * row, element (row, col) at offset row * n + col. The leading dimensions
+ * lda, ldb, ldc generalise that row length n. Work: Chapter 9, Optimised
+ * Matrix Multiplication, section 9.1 — M*N*K multiply-adds, 2*M*N*K FLOPs.
+ *
+ * Conventions fixed by this library where the pages are silent:
+ *   - C is overwritten and never read (no alpha/beta scaling): every listing
+ *     on the pages ends with a plain assignment of the sum to C.
+ *   - Entries of a C row between column N and ldc are never touched.
+ *   - K == 0 writes zeros to C (the empty sum); M == 0 or N == 0 is a no-op.
+ *   - Arithmetic is IEEE FP32 with round-to-nearest fused multiply-adds,
+ *     denormals kept, NaN/Inf propagated; the order of the K-sum is not
+ *     specified (results are not bit-identical across kernel configs on
+ *     general float inputs; they are on integer-valued inputs whose partial
+ *     sums stay below 2^24 in magnitude).
+ *
+ * Layout: all matrices are row-major FP32 in device memory (HBM).
+ * Ownership: every pointer is caller-owned device memory; the library never
+ * frees, retains or reads host memory through it. Scratch space the library
+ * needs (a packed copy of an operand whose rows are not 16-byte aligned) is
+ * taken from a library-owned, stream-ordered memory pool on `stream` and
+ * returned on `stream`; it is never exposed.
+ * Asynchrony: calls return after enqueueing work on `stream`; results are
+ * ready when the stream's work completes. A call enqueues at most three
+ * kernels (operand packing, then the product) and no host synchronisation.
+ * Thread safety: calls on different host threads/streams are safe.
+ */
+#ifndef DENSE_FP32_MATRIX_07_GB300_SGEMM_H
+#define DENSE_FP32_MATRIX_07_GB300_SGEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. Every nonzero code returned by sgemm()/sgemm_ex() means that
+ * nothing was enqueued on the stream and C is untouched. */
+enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_VALUE = 1, /* negative size, short leading dimension,
+                                    NULL pointer with a non-empty extent,
+                                    C overlapping A or B, unknown config */
+    SGEMM_ERR_OVERFLOW = 2,      /* an index or byte offset would overflow,
+                                    or a size exceeds the kernels' 2^31-1
+                                    coordinate range */
+    SGEMM_ERR_ALLOC = 3,         /* scratch allocation failed */
+    SGEMM_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError) */
+    SGEMM_ERR_TIMEOUT = 5,       /* a device-side wait hit its bounded spin
+                                    limit; reported by sgemm_check_status() */
+    SGEMM_ERR_CUDA = 6,          /* another CUDA runtime failure (no device,
+                                    device query, sticky context error) */
+    SGEMM_ERR_UNSUPPORTED = 7    /* the forced config cannot run this problem */
+};
+
+/*
+ * sgemm — C = A . B (see the top of this file for the exact semantics).
+ *
+ *   M, N, K   problem sizes, >= 0.
+ *   A         device pointer, M rows of K floats, row i at A + i*lda;
+ *             lda >= max(1, K). May be NULL when M == 0, N == 0 or K == 0.
+ *   B         device pointer, K rows of N floats, row k at B + k*ldb;
+ *             ldb >= max(1, N). May be NULL when M == 0, N == 0 or K == 0.
+ *   C         device pointer, M rows of N floats, row i at C + i*ldc;
+ *             ldc >= max(1, N). Must not overlap A or B. May be NULL only
+ *             when M == 0 or N == 0.
+ *   stream    CUDA stream to enqueue on (0 = the legacy default stream).
+ *
+ * Any alignment of A, B, C and any leading dimension is accepted. Operands
+ * whose base address is 16-byte aligned and whose leading dimension is a
+ * multiple of 4 floats are read in place by the tensor-memory-accelerator
+ * (TMA) path; others are first packed into aligned scratch. C is written with
+ * 16-byte vector stores when it is aligned the same way, else with scalar
+ * stores.
+ *
+ * Returns SGEMM_OK or one of the codes above. A device-side timeout cannot
+ * be known when the call returns; see sgemm_check_status().
+ */
+int sgemm(int64_t M, int64_t N, int64_t K,
+          const float *A, int64_t lda,
+          const float *B, int64_t ldb,
+          float *C, int64_t ldc,
+          cudaStream_t stream);
+
+/*
+ * sgemm_ex — sgemm() with an explicit kernel configuration.
+ *
+ *   config    -1 picks the configuration automatically (exactly sgemm());
+ *             0 .. sgemm_num_configs()-1 forces that configuration.
+ *
+ * Returns SGEMM_ERR_INVALID_VALUE for an unknown config and
+ * SGEMM_ERR_UNSUPPORTED when the forced config cannot run the problem.
+ * Intended for tests and tuning sweeps.
+ */
+int sgemm_ex(int64_t M, int64_t N, int64_t K,
+             const float *A, int64_t lda,
+             const float *B, int64_t ldb,
+             float *C, int64_t ldc,
+             int config, cudaStream_t stream);
+
+/*
+ * sgemm_check_status — waits for `stream`, then reads and clears the current
+ * device's error word. Returns SGEMM_ERR_TIMEOUT if any kernel of this
+ * library on the device gave up a bounded wait since the last check (its
+ * output is then incomplete), SGEMM_ERR_CUDA if the stream reports a CUDA
+ * error, else SGEMM_OK. The error word is per device, not per stream.
+ */
+int sgemm_check_status(cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *sgemm_error_string(int code);
+
+/* Number of kernel configurations that sgemm_ex() accepts. */
+int sgemm_num_configs(void);
+
+/* Static name of configuration `config` ("?" when out of range). */
+const char *sgemm_config_name(int config);
+
+/*
+ * sgemm_plan — host-only view of the choice sgemm() makes; needs no GPU.
+ *
+ *   a_addr, b_addr, c_addr   the operand addresses (only their alignment
+ *                            matters; 0 means aligned).
+ *   num_sms                  streaming multiprocessors of the target device.
+ *   out_config               (nullable) receives the chosen configuration.
+ *   out_pack_a, out_pack_b   (nullable) receive 1 if that operand would be
+ *                            packed into scratch first, else 0.
+ *
+ * Returns SGEMM_OK, or the code sgemm() would return for invalid sizes.
+ */
+int sgemm_plan(int64_t M, int64_t N, int64_t K,
+               int64_t lda, int64_t ldb, int64_t ldc,
+               uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+               int num_sms,
+               int *out_config, int *out_pack_a, int *out_pack_b);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_FP32_MATRIX_07_GB300_SGEMM_H */

@@ -1,0 +1,100 @@
+"""C-ABI library: loads without a GPU, exports every declared symbol, and its
+host-only logic (status strings, config table, the planner) behaves. No
+compute call is made here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp32_matrix_07_gb300 as sg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "sgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_functions():
+    assert declared_functions() == sorted(sg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(sgemm_lib):
+    for name in declared_functions():
+        assert hasattr(sgemm_lib, name), name
+        assert isinstance(getattr(sgemm_lib, name), ctypes._CFuncPtr)
+
+
+def test_library_links_no_cuda_driver_or_runtime_dynamically():
+    # The CUDA runtime is linked statically and the driver is reached through
+    # the runtime's entry-point query, so the library loads on any host.
+    import subprocess
+    out = subprocess.run(["ldd", sg.library_path()], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart" not in out, out
+
+
+def test_error_strings():
+    for code in range(8):
+        s = sg.sgemm_error_string(code)
+        assert s and s != "unknown sgemm status code"
+    assert sg.sgemm_error_string(99) == "unknown sgemm status code"
+    assert sg.sgemm_error_string(sg.SGEMM_ERR_TIMEOUT).startswith("SGEMM_ERR_TIMEOUT")
+
+
+def test_config_table():
+    n = sg.sgemm_num_configs()
+    assert n >= 2
+    names = [sg.sgemm_config_name(i) for i in range(n)]
+    assert len(set(names)) == n and "?" not in names
+    assert names[0] == "tiled16_simple"
+    assert sg.sgemm_config_name(n) == "?" and sg.sgemm_config_name(-1) == "?"
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, 4, 4, 4), sg.SGEMM_ERR_INVALID_VALUE),
+    ((4, -1, 4, 4, 4, 4), sg.SGEMM_ERR_INVALID_VALUE),
+    ((4, 4, -1, 4, 4, 4), sg.SGEMM_ERR_INVALID_VALUE),
+    ((4, 4, 4, 3, 4, 4), sg.SGEMM_ERR_INVALID_VALUE),   # lda < K
+    ((4, 4, 4, 4, 3, 4), sg.SGEMM_ERR_INVALID_VALUE),   # ldb < N
+    ((4, 4, 4, 4, 4, 3), sg.SGEMM_ERR_INVALID_VALUE),   # ldc < N
+    ((4, 4, 0, 0, 4, 4), sg.SGEMM_OK),                  # K = 0: lda, ldb unused
+    ((0, 4, 4, 0, 0, 0), sg.SGEMM_OK),                  # M = 0: nothing to do
+    ((2 ** 31, 4, 4, 4, 4, 4), sg.SGEMM_ERR_OVERFLOW),  # beyond 32-bit coordinates
+    ((2 ** 30, 4, 4, 2 ** 62, 4, 4), sg.SGEMM_ERR_OVERFLOW),  # byte extent overflows
+])
+def test_plan_validates_sizes(args, code):
+    rc, *_ = sg.sgemm_plan(*args, 0, 0, 0, 148)
+    assert rc == code
+
+
+def test_plan_packs_only_misaligned_operands():
+    # Aligned operands with 16-byte rows: read in place.
+    rc, cfg, pa, pb = sg.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, 0, 0, 0, 148)
+    assert rc == 0 and (pa, pb) == (0, 0)
+    # Rows that are not a multiple of 16 bytes (the 4097x3001x2049 workload).
+    rc, cfg, pa, pb = sg.sgemm_plan(4097, 3001, 2049, 2049, 3001, 3001, 0, 0, 0, 148)
+    assert rc == 0 and (pa, pb) == (1, 1)
+    # A misaligned base address alone forces a pack of that operand.
+    rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 4, 0, 0, 148)
+    assert rc == 0 and (pa, pb) == (1, 0)
+    rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 0, 8, 12, 148)
+    assert rc == 0 and (pa, pb) == (0, 1)
+
+
+def test_plan_picks_smaller_tiles_when_the_grid_would_be_underfilled():
+    rc, big, *_ = sg.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, 0, 0, 0, 148)
+    rc2, small, *_ = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 0, 0, 0, 148)
+    assert rc == rc2 == 0
+    assert big != small
+    assert sg.sgemm_config_name(big).startswith("ffma")
+    assert sg.sgemm_config_name(small).startswith("ffma")
+
+
+def test_plan_rejects_nonpositive_sm_count():
+    rc, *_ = sg.sgemm_plan(4, 4, 4, 4, 4, 4, 0, 0, 0, 0)
+    assert rc == sg.SGEMM_ERR_INVALID_VALUE

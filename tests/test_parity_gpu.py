@@ -1,0 +1,193 @@
+"""GPU parity: the CUDA library (through its C ABI) against the FP64 oracle.
+
+Covers every kernel configuration on a shape sweep with ragged tails,
+integer-valued inputs (bit-exact), strides beyond the row length, misaligned
+pointers (the pack path), a NaN-prefilled C (C is never read), guard bands
+(no write outside C's rows), the degenerate sizes, and the named workloads
+at their full sizes (full checks up to 4097x3001x2049, sampled rows and
+columns at 4096 and 16384).
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import dense_fp32_matrix_07_gb300 as sg
+import workloads
+from gpu_util import DeviceMatrix, assert_parity, check_untouched_padding, run
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = list(range(sg.sgemm_num_configs()))
+CFG_IDS = [sg.sgemm_config_name(i) for i in CONFIGS]
+EDGE = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257]
+
+
+def _oracle_check(oracle, M, N, K, A, lda, B, ldb, C, exact, what):
+    Cref, S = oracle.sgemm(M, N, K, A.numpy(), lda, B.numpy(), ldb)
+    return assert_parity(C, Cref, S, exact, what)
+
+
+def _shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    out = {(1, 1, 1), (257, 257, 257), (129, 1, 33), (1, 257, 129), (33, 17, 1)}
+    while len(out) < n:
+        out.add(tuple(int(x) for x in rng.choice(EDGE, 3)))
+    return sorted(out)
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+def test_shape_sweep_float(cuda_device, oracle, config):
+    for n, (M, N, K) in enumerate(_shapes(1000 + config, 40)):
+        A, B = workloads.make_operands(M, N, K, "uniform", n)
+        rc, C, dC = run(M, N, K, A, K, B, N, config=config)
+        assert rc == 0, (M, N, K, sg.sgemm_error_string(rc))
+        _oracle_check(oracle, M, N, K, A, K, B, N, C, False, f"cfg {config} {M}x{N}x{K}")
+        check_untouched_padding(dC, N)
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+def test_shape_sweep_integer_exact(cuda_device, oracle, config):
+    for n, (M, N, K) in enumerate(_shapes(2000 + config, 25)):
+        A, B = workloads.make_operands(M, N, K, "int", 50 + n)
+        rc, C, _ = run(M, N, K, A, K, B, N, config=config)
+        assert rc == 0
+        _oracle_check(oracle, M, N, K, A, K, B, N, C, True, f"cfg {config} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("shape", [(300, 200, 100), (517, 389, 1000), (1024, 1024, 1024)])
+def test_multi_tile_ragged(cuda_device, oracle, config, shape):
+    M, N, K = shape
+    for dist, exact in (("normal", False), ("int", True)):
+        A, B = workloads.make_operands(M, N, K, dist, 7)
+        rc, C, dC = run(M, N, K, A, K, B, N, config=config)
+        assert rc == 0
+        _oracle_check(oracle, M, N, K, A, K, B, N, C, exact, f"cfg {config} {shape} {dist}")
+        check_untouched_padding(dC, N)
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+def test_strides_beyond_row_length(cuda_device, oracle, config):
+    M, N, K = 133, 70, 91
+    for lda, ldb, ldc in [(K + 5, N + 3, N + 7), (K + 3, N + 10, N + 4), (128, 72, 96)]:
+        A, B = workloads.make_operands(M, N, K, "uniform", 3, lda=lda, ldb=ldb)
+        rc, C, dC = run(M, N, K, A, lda, B, ldb, ldc=ldc, config=config)
+        assert rc == 0
+        _oracle_check(oracle, M, N, K, A, lda, B, ldb, C, False, f"cfg {config} ld {lda},{ldb},{ldc}")
+        check_untouched_padding(dC, N)
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 2, 0), (0, 0, 3), (3, 1, 2)])
+def test_misaligned_pointers(cuda_device, oracle, config, offsets):
+    M, N, K = 100, 130, 70
+    A, B = workloads.make_operands(M, N, K, "normal", 4)
+    rc, C, dC = run(M, N, K, A, K, B, N, config=config, offsets=offsets)
+    assert rc == 0
+    _oracle_check(oracle, M, N, K, A, K, B, N, C, False, f"cfg {config} offsets {offsets}")
+    check_untouched_padding(dC, N)
+
+
+@pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
+def test_nan_in_a_row_propagates(cuda_device, config):
+    M, N, K = 160, 150, 140
+    A, B = workloads.make_operands(M, N, K, "uniform", 5)
+    A[37, 11] = float("nan")
+    rc, C, _ = run(M, N, K, A, K, B, N, config=config, c_fill=0.0)
+    assert rc == 0
+    assert torch.isnan(C[37]).all()
+    assert not torch.isnan(torch.cat([C[:37], C[38:]])).any()
+
+
+def test_k_zero_writes_zeros(cuda_device):
+    M, N = 37, 45
+    rc, C, dC = run(M, N, 0, torch.zeros(1), 1, torch.zeros(1), N, ldc=N + 3)
+    assert rc == 0
+    assert bool((C == 0).all())
+    check_untouched_padding(dC, N)
+
+
+@pytest.mark.parametrize("M,N", [(0, 5), (5, 0), (0, 0)])
+def test_empty_output_is_a_noop(cuda_device, M, N):
+    dC = DeviceMatrix(None, 4, 8, 8)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert sg.sgemm(M, N, 3, 0, 3, 0, max(N, 1), dC.ptr, max(N, 1), stream) == 0
+    torch.cuda.synchronize()
+    assert dC.guard_intact() and bool((dC.matrix() == 12345.678).all())
+
+
+def test_invalid_arguments_launch_nothing(cuda_device):
+    M, N, K = 8, 8, 8
+    A, B = workloads.make_operands(M, N, K, "uniform", 1)
+    dA, dB = DeviceMatrix(A, M, K, K), DeviceMatrix(B, K, N, N)
+    dC = DeviceMatrix(None, M, N, N)
+    s = torch.cuda.current_stream().cuda_stream
+    E = sg.SGEMM_ERR_INVALID_VALUE
+    cases = [
+        ((-1, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N), E),
+        ((M, N, K, dA.ptr, K - 1, dB.ptr, N, dC.ptr, N), E),
+        ((M, N, K, dA.ptr, K, dB.ptr, N - 1, dC.ptr, N), E),
+        ((M, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N - 1), E),
+        ((M, N, K, 0, K, dB.ptr, N, dC.ptr, N), E),
+        ((M, N, K, dA.ptr, K, 0, N, dC.ptr, N), E),
+        ((M, N, K, dA.ptr, K, dB.ptr, N, 0, N), E),
+        ((M, N, K, dA.ptr, K, dB.ptr, N, dA.ptr + 16, N), E),   # C overlaps A
+        ((M, N, K, dA.ptr, K, dB.ptr, N, dB.ptr, N), E),        # C aliases B
+        ((2 ** 31, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N), sg.SGEMM_ERR_OVERFLOW),
+    ]
+    for args, code in cases:
+        assert sg.sgemm(*args, s) == code, args
+    assert sg.sgemm_ex(M, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N, sg.sgemm_num_configs(), s) == E
+    torch.cuda.synchronize()
+    assert bool((dC.matrix() == 12345.678).all()), "a rejected call wrote C"
+    assert sg.sgemm_check_status(s) == 0
+
+
+# --------------------------------------------------------------------------
+# The named workloads at their full sizes, through sgemm() (automatic config,
+# the launch the bench times).
+# --------------------------------------------------------------------------
+
+def _run_workload(w, dist=None):
+    dist = dist or w.dist
+    A, B = workloads.make_operands(w.M, w.N, w.K, dist, w.seed, w.lda, w.ldb)
+    rc, C, dC = run(w.M, w.N, w.K, A, w.lda, B, w.ldb, ldc=w.ldc, c_fill=float("nan"))
+    assert rc == 0
+    check_untouched_padding(dC, w.N)
+    return A, B, C
+
+
+@pytest.mark.parametrize("name", ["sq256", "sq256_int", "sq1024", "sq1024_int", "rect4097x3001x2049"])
+def test_workload_full_check(cuda_device, oracle, name):
+    w = workloads.WORKLOADS[name]
+    A, B, C = _run_workload(w)
+    r = _oracle_check(oracle, w.M, w.N, w.K, A, w.lda, B, w.ldb, C, w.dist == "int", name)
+    print(f"{name}: max |diff|/S = {r:.3e}")
+
+
+def _sampled_check(oracle, w, A, B, C, exact):
+    rows = workloads.sample_indices(w.M, 256, w.seed + 1000)
+    cols = workloads.sample_indices(w.N, 256, w.seed + 2000)
+    Cr, Sr = oracle.sgemm_rows(w.M, w.N, w.K, A.numpy(), w.lda, B.numpy(), w.ldb, rows)
+    Cc, Sc = oracle.sgemm_cols(w.M, w.N, w.K, A.numpy(), w.lda, B.numpy(), w.ldb, cols)
+    r1 = assert_parity(C[torch.from_numpy(rows)], Cr, Sr, exact, f"{w.name} rows")
+    r2 = assert_parity(C[:, torch.from_numpy(cols)], Cc, Sc, exact, f"{w.name} cols")
+    return max(r1, r2)
+
+
+@pytest.mark.parametrize("name,dist", [("sq4096", None), ("sq4096", "int"),
+                                       ("rect4097x3001x2049", "int"), ("sq16384", None)])
+def test_workload_sampled_check(cuda_device, oracle, name, dist):
+    w = workloads.WORKLOADS[name]
+    A, B, C = _run_workload(w, dist)
+    r = _sampled_check(oracle, w, A, B, C, dist == "int")
+    print(f"{name} {dist or w.dist}: max |diff|/S = {r:.3e}")
+    del A, B, C
+    torch.cuda.empty_cache()
+
+
+def test_status_is_clean_after_the_suite(cuda_device):
+    assert sg.sgemm_check_status(torch.cuda.current_stream().cuda_stream) == sg.SGEMM_OK
