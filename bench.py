@@ -26,6 +26,7 @@ Also reported on the same JSON line:
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -35,6 +36,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import uuid
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -126,20 +128,28 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 11:
+            # timestamp, index, clocks.sm, clocks.max.sm, power.draw, active,
+            # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+            if len(parts) < 10:
                 continue
             try:
-                rows.append({"sm": float(parts[2]), "max": float(parts[3]),
-                             "hw": parts[7], "hw_thermal": parts[8], "sw_thermal": parts[9],
-                             "sw_power": parts[10]})
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power": parts[9]})
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return None
-        # Samples under load: the SM clock near its busy value; the first and
-        # last samples bracket the timed region.
-        load = [r for r in rows if r["sm"] >= 0.5 * r["max"]] or rows
+        # Samples taken inside the timed region (host and nvidia-smi share the
+        # clock); if the region was shorter than the sampling period, the
+        # samples nearest to it.
+        inside = [r for r in rows if self.t_start - 0.03 <= r["t"] <= self.t_end + 0.03]
+        if not inside:
+            mid = 0.5 * (self.t_start + self.t_end)
+            inside = sorted(rows, key=lambda r: abs(r["t"] - mid))[:2]
+        load = inside
         reasons = set()
         for r in load:
             for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
@@ -155,10 +165,12 @@ def nvsmi_gpu_id(dev, local: int) -> str:
     """nvidia-smi's id of this process's GPU (its UUID when torch knows it)."""
     import torch
     try:
-        u = str(torch.cuda.get_device_properties(dev).uuid)
-        if u:
+        raw = torch.cuda.get_device_properties(dev).uuid
+        b = raw.bytes if hasattr(raw, "bytes") else None
+        u = str(uuid.UUID(bytes=bytes(b))) if b is not None and len(b) == 16 else str(raw)
+        if re.fullmatch(r"(GPU-)?[0-9a-fA-F-]{36}", u):
             return u if u.startswith("GPU-") else "GPU-" + u
-    except (AttributeError, RuntimeError):
+    except (AttributeError, RuntimeError, ValueError, TypeError):
         pass
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     parts = [p for p in vis.split(",") if p.strip()]
@@ -207,7 +219,7 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, "cpu_oracle_f64"),
+        "config": workload_config(w, "cpu_oracle_f64", l2="host CPU: no GPU cache involved"),
         "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
@@ -220,13 +232,14 @@ def run_reference(args, world, rank):
 METRIC = "SGEMM GFLOP/s at N=4096 FP32 and % of GB300 FP32 FFMA peak"
 
 
-def workload_config(w, kernel):
+def workload_config(w, kernel, l2=None):
     total = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
+    if l2 is None:
+        l2 = (f"A+B+C = {total / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"
+              if total > L2_BYTES else
+              f"A+B+C = {total / 1e6:.1f} MB: L2 flushed between steps")
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.lda, "ldb": w.ldb,
-            "ldc": w.ldc, "dist": w.dist, "seed": w.seed, "kernel": kernel,
-            "l2": (f"A+B+C = {total / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2, no flush"
-                   if total > L2_BYTES else
-                   f"A+B+C = {total / 1e6:.1f} MB: L2 flushed between steps")}
+            "ldc": w.ldc, "dist": w.dist, "seed": w.seed, "kernel": kernel, "l2": l2}
 
 
 def cpu_baseline(w, A, B):
