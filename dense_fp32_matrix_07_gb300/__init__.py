@@ -26,10 +26,11 @@ SGEMM_ERR_LAUNCH = 4
 SGEMM_ERR_TIMEOUT = 5
 SGEMM_ERR_CUDA = 6
 SGEMM_ERR_UNSUPPORTED = 7
+SGEMM_ERR_SCRATCH_LIMIT = 8
 
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
-            "sgemm_num_configs", "sgemm_config_name", "sgemm_plan")
+            "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +57,8 @@ def load(rebuild: bool = False):
             lib.sgemm_ex.restype = ctypes.c_int
             lib.sgemm_ex.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                      ctypes.c_int, _vp]
+            lib.sgemm_noalloc.restype = ctypes.c_int
+            lib.sgemm_noalloc.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
             lib.sgemm_check_status.restype = ctypes.c_int
             lib.sgemm_check_status.argtypes = [_vp]
             lib.sgemm_error_string.restype = ctypes.c_char_p
@@ -87,6 +90,15 @@ def sgemm(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 def sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, config, stream=0) -> int:
     """sgemm() with a forced kernel configuration (-1 = automatic)."""
     return load().sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, config, stream)
+
+
+def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """sgemm() for callers that cannot allocate: misaligned operands are
+    packed into the library's fixed 64 MiB scratch array instead of
+    allocated scratch; returns SGEMM_ERR_SCRATCH_LIMIT if they would not
+    fit. All calls on a device share that array, so calls that overlap on
+    the GPU race on it."""
+    return load().sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def sgemm_check_status(stream=0) -> int:

@@ -29,6 +29,9 @@ enum : unsigned int {
 // orders of magnitude above any legitimate wait in these kernels.
 constexpr unsigned int kSpinLimit = 1u << 23;
 
+// Device address of the current device's error word.
+cudaError_t device_status_word(unsigned int **out);
+
 // Launchers (each returns the launch's cudaGetLastError()).
 cudaError_t launch_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc,
                              cudaStream_t stream);

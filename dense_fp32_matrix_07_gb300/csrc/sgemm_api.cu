@@ -116,6 +116,12 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
+// Device address of this device's error word (no allocation involved).
+cudaError_t device_status_word(unsigned int **out)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_status_word);
+}
+
 // Operand of a product that the TMA path reads in place only when its base
 // is 16-byte aligned and its rows are a multiple of 16 bytes long.
 static bool needs_pack(uint64_t addr, int64_t ld) { return !is_aligned16(addr) || (ld % 4) != 0; }
@@ -145,6 +151,7 @@ const char *sgemm_error_string(int code)
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a device-side wait hit its spin limit";
     case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: CUDA runtime failure";
     case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: the forced config cannot run this problem";
+    case SGEMM_ERR_SCRATCH_LIMIT: return "SGEMM_ERR_SCRATCH_LIMIT: packed operands exceed sgemm_noalloc's 64 MiB scratch array";
     default: return "unknown sgemm status code";
     }
 }

@@ -61,7 +61,9 @@ enum {
                                     limit; reported by sgemm_check_status() */
     SGEMM_ERR_CUDA = 6,          /* another CUDA runtime failure (no device,
                                     device query, sticky context error) */
-    SGEMM_ERR_UNSUPPORTED = 7    /* the forced config cannot run this problem */
+    SGEMM_ERR_UNSUPPORTED = 7,   /* the forced config cannot run this problem */
+    SGEMM_ERR_SCRATCH_LIMIT = 8  /* sgemm_noalloc(): the packed operands would
+                                    not fit its fixed scratch array */
 };
 
 /*
@@ -144,6 +146,42 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K,
                uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
                int num_sms,
                int *out_config, int *out_pack_a, int *out_pack_b);
+
+/*
+ * sgemm_noalloc — sgemm() for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for users of
+ * this library. Some callers cannot call cudaMalloc (or any allocating
+ * routine, torch's caching allocator included) where they need a product:
+ * code whose device memory is fully handed to another allocator or to a
+ * fixed-size arena, and latency-critical loops that must not take the
+ * driver's allocation path (which can block and synchronise). sgemm() itself
+ * allocates only when an operand needs packing (a base address that is not
+ * 16-byte aligned, or a leading dimension that is not a multiple of 4
+ * floats); this entry point packs such operands into a fixed scratch array
+ * compiled into the library instead, and allocates nothing.
+ *
+ * Arguments, semantics, ownership and status codes: as sgemm().
+ *
+ * Limit: the packed operands must fit the 64 MiB array (16 Mi floats):
+ * M * round_up(K, 32) floats for a packed A plus K * round_up(N, 32) floats
+ * for a packed B. Larger requests return SGEMM_ERR_SCRATCH_LIMIT with nothing
+ * enqueued. Aligned operands are not packed and have no size limit.
+ *
+ * Memory: every GPU that loads the library's device code holds the 64 MiB
+ * array until the process exits.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address and caches it with the device's other constants;
+ * make that first call before any stream capture begins.
+ * Sharing: all calls on a device share the one array, which keeps the last
+ * call's packed data; calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on it, so the caller must order them.
+ */
+int sgemm_noalloc(int64_t M, int64_t N, int64_t K,
+                  const float *A, int64_t lda,
+                  const float *B, int64_t ldb,
+                  float *C, int64_t ldc,
+                  cudaStream_t stream);
 
 #ifdef __cplusplus
 }
