@@ -6,6 +6,13 @@
 
 namespace sgemm_gb300 {
 
+// How the TMA kernels divide the output tiles among their CTAs.
+enum SchedPolicy : int {
+    kSchedAuto = 0,          // whole tiles, or stream-K when the last wave is short
+    kSchedDataParallel = 1,  // whole tiles only (needs no workspace)
+    kSchedStreamK = 2        // every tile's K slabs shared out evenly (tests)
+};
+
 // Arguments of one product C = A . B (row-major, FP32, device pointers).
 struct GemmArgs {
     int64_t M, N, K;
@@ -17,6 +24,9 @@ struct GemmArgs {
     int64_t ldc;
     unsigned int *status;  // device error word of the current device
     int num_sms;           // streaming multiprocessors of the current device
+    int sched = kSchedDataParallel;
+    void *workspace = nullptr;     // stream-K partial sums and flags, or null
+    size_t workspace_bytes = 0;
 };
 
 // Bits of the device error word.
@@ -24,10 +34,11 @@ enum : unsigned int {
     kStatusTimeout = 1u,   // a bounded wait gave up
 };
 
-// Spin limit of every device-side wait. Each failed try_wait sleeps up to
-// ~256 ns, so the limit corresponds to roughly a second or two of waiting,
-// orders of magnitude above any legitimate wait in these kernels.
-constexpr unsigned int kSpinLimit = 1u << 23;
+// Probe-count backstop of the device-side waits. Their primary bound is wall
+// clock (about a second of %globaltimer time, orders of magnitude above any
+// legitimate wait in these kernels); this caps the number of probe rounds in
+// case the timer were not to advance.
+constexpr unsigned int kSpinLimit = 1u << 20;
 
 // Device address of the current device's error word.
 cudaError_t device_status_word(unsigned int **out);

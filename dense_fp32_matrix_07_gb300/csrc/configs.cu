@@ -4,11 +4,16 @@
 namespace sgemm_gb300 {
 
 const ConfigInfo kConfigTable[kNumConfigs] = {
-    {"tiled16_simple", false, 16, 16},
-    {"ffma_128x128_k32_s4", true, 128, 128},
-    {"ffma2_128x128_k32_s4", true, 128, 128},
-    {"ffma2_128x128_k16_s8", true, 128, 128},
-    {"ffma2_128x64_k32_s4", true, 128, 64},
+    {"tiled16_simple", kKernTiledSimple, kSchedDataParallel, false, 16, 16},
+    {"ffma_128x128_k32_s4", kKernFfma128x128k32s4, kSchedAuto, true, 128, 128},
+    {"ffma2_128x128_k32_s4", kKernFfma2_128x128k32s4, kSchedAuto, true, 128, 128},
+    {"ffma2_128x128_k16_s8", kKernFfma2_128x128k16s8, kSchedAuto, true, 128, 128},
+    {"ffma2_128x64_k32_s4", kKernFfma2_128x64k32s4, kSchedAuto, true, 128, 64},
+    {"ffma2_128x256_k32_s4", kKernFfma2_128x256k32s4, kSchedAuto, true, 128, 256},
+    {"ffma2_128x128_k32_s4_dp", kKernFfma2_128x128k32s4, kSchedDataParallel, true, 128, 128},
+    {"ffma2_128x128_k32_s4_sk", kKernFfma2_128x128k32s4, kSchedStreamK, true, 128, 128},
+    {"ffma2_128x256_k32_s4_dp", kKernFfma2_128x256k32s4, kSchedDataParallel, true, 128, 256},
+    {"ffma2_128x256_k32_s4_sk", kKernFfma2_128x256k32s4, kSchedStreamK, true, 128, 256},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
@@ -23,18 +28,32 @@ bool config_supports(int cfg, const ProblemShape &p)
 
 int select_config(const ProblemShape &p)
 {
-    // Work per SM decides between the two block shapes: when 128x128 tiles
-    // would leave SMs idle, the half-width tile doubles the CTA count.
+    if (!config_supports(kCfgFfma2_128x128, p)) return kCfgTiledSimple;
+    // The widest thread tile (8x16) when there are enough 128x256 tiles to
+    // give every SM one; below that, 128x128, and 128x64 (two CTAs per SM)
+    // when even 128x128 tiles cannot fill the SMs. The stream-K tail evens
+    // out partial last waves in all three.
+    const int64_t tiles256 = ((p.M + 127) / 128) * ((p.N + 255) / 256);
     const int64_t tiles128 = ((p.M + 127) / 128) * ((p.N + 127) / 128);
-    if (!config_supports(kCfgFfma2_128x128k32s4, p)) return kCfgTiledSimple;
-    if (tiles128 < p.num_sms) return kCfgFfma2_128x64k32s4;
-    return kCfgFfma2_128x128k32s4;
+    if (tiles256 >= p.num_sms) return kCfgFfma2_128x256;
+    if (tiles128 >= p.num_sms) return kCfgFfma2_128x128;
+    return kCfgFfma2_128x64;
+}
+
+size_t config_workspace_bytes(int cfg, const GemmArgs &g)
+{
+    if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].uses_tma) return 0;
+    GemmArgs a = g;
+    a.sched = kConfigTable[cfg].sched;
+    return ffma_tma_workspace_bytes(kConfigTable[cfg].kernel, a);
 }
 
 cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
-    if (cfg == kCfgTiledSimple) return launch_tiled_simple(g, stream);
-    return launch_ffma_tma(cfg, g, stream);
+    if (kConfigTable[cfg].kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
+    GemmArgs a = g;
+    if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
+    return launch_ffma_tma(kConfigTable[cfg].kernel, a, stream);
 }
 
 cudaError_t configs_prepare_device() { return prepare_ffma_tma(); }

@@ -16,19 +16,37 @@ struct ProblemShape {
     int num_sms;
 };
 
+// Kernel instances.
+enum KernelId : int {
+    kKernTiledSimple = 0,       // predicated 16x16 shared-memory tiles, any layout
+    kKernFfma128x128k32s4,      // TMA ring, 128x128 block, BK 32, 4 stages, FFMA
+    kKernFfma2_128x128k32s4,    // same, paired FFMA2
+    kKernFfma2_128x128k16s8,    // 128x128 block, BK 16, 8 stages, FFMA2
+    kKernFfma2_128x64k32s4,     // 128x64 block (4 consumer warps), 2 CTAs per SM
+    kKernFfma2_128x256k32s4,    // 128x256 block, 8x16 thread tiles, FFMA2
+};
+
+// Configurations = kernel instance + schedule policy.
 enum ConfigId : int {
-    kCfgTiledSimple = 0,       // predicated 16x16 shared-memory tiles, any layout
-    kCfgFfma128x128k32s4,      // TMA ring, 128x128 block, BK 32, 4 stages, FFMA
-    kCfgFfma2_128x128k32s4,    // same, paired FFMA2
-    kCfgFfma2_128x128k16s8,    // 128x128 block, BK 16, 8 stages, FFMA2
-    kCfgFfma2_128x64k32s4,     // 128x64 block (4 consumer warps), BK 32, 4 stages, 2 CTAs per SM
+    kCfgTiledSimple = 0,
+    kCfgFfma128x128,
+    kCfgFfma2_128x128,
+    kCfgFfma2_128x128k16,
+    kCfgFfma2_128x64,
+    kCfgFfma2_128x256,
+    kCfgFfma2_128x128_dp,
+    kCfgFfma2_128x128_sk,
+    kCfgFfma2_128x256_dp,
+    kCfgFfma2_128x256_sk,
     kNumConfigs
 };
 
 struct ConfigInfo {
     const char *name;
+    int kernel;      // KernelId
+    int sched;       // SchedPolicy
     bool uses_tma;   // reads A and B through TMA tensor maps
-    int bm, bn;      // block tile (0 for the simple kernel's 16x16)
+    int bm, bn;      // block tile
 };
 
 extern const ConfigInfo kConfigTable[kNumConfigs];
@@ -37,16 +55,22 @@ extern const ConfigInfo kConfigTable[kNumConfigs];
 int select_config(const ProblemShape &p);
 bool config_supports(int cfg, const ProblemShape &p);
 
+// Workspace bytes configuration `cfg` wants for this product (0: none).
+size_t config_workspace_bytes(int cfg, const GemmArgs &g);
+
 // Runs configuration `cfg` on operands that already satisfy its alignment
 // needs (the API packs misaligned operands for TMA configurations first).
+// g.sched is overwritten with the configuration's policy unless it is
+// kSchedDataParallel; without g.workspace the schedule is whole tiles.
 cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream);
 
 // One-time per-device set-up (shared-memory limits of the kernels, the
 // tensor-map encoder); call with the device current.
 cudaError_t configs_prepare_device();
 
-// Launchers of the TMA kernels (kernels_ffma_tma.cu).
-cudaError_t launch_ffma_tma(int cfg, const GemmArgs &g, cudaStream_t stream);
+// Launchers of the TMA kernels (kernels_ffma_tma.cu), by KernelId.
+cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream);
+size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g);
 cudaError_t prepare_ffma_tma();
 
 }  // namespace sgemm_gb300

@@ -5,8 +5,8 @@
 //  * The CUDA Handbook, ch.17, section 17.3 (Cache Blocking) and Figure 17-2:
 //    a thread block owns a BM x BN tile of C and marches K in BK-deep slabs;
 //    each thread keeps a TM x TN micro-tile of accumulators in registers
-//    (8 x 8 was the best there), so one loaded strip of A and of B feeds 64
-//    multiply-adds.
+//    (8 x 8 was the best there), so one loaded strip of A and of B feeds
+//    TM*TN multiply-adds.
 //  * Chapter 9: Optimised Matrix Multiplication, sections 9.4-9.6: slabs are
 //    staged in shared memory once per block and reused, bank conflicts are
 //    designed out, and registers per thread are traded against occupancy by
@@ -19,15 +19,29 @@
 // every consumer warp has finished with it), which replace the pages' two
 // __syncthreads() per phase. The A slab uses the TMA 128-byte (BK 32) or
 // 64-byte (BK 16) swizzle instead of the pages' +1 padding column, which
-// TMA cannot produce. The grid is persistent (one CTA per SM) and walks the
-// output tiles in groups of 8 block rows so concurrently running CTAs share
-// A and B panels in L2. Zero fill of out-of-range boxes by TMA handles the
-// M, N and K tails; the epilogue predicates its stores.
+// TMA cannot produce. Zero fill of out-of-range boxes by TMA handles the M, N
+// and K tails; the epilogue predicates its stores.
 //
-// Every mbarrier wait is bounded in time (about a second): on giving up, the
-// thread sets the device error word (read by sgemm_check_status()) and
-// returns; the producer first waits (bounded as well) for every copy it has
-// issued, so no copy can land in the shared memory of an exited CTA.
+// Work schedule (persistent grid, at most one CTA per SM and resident slot):
+// output tiles are numbered in groups of 8 block rows (so CTAs running at the
+// same time share A and B panels in L2). Tiles [0, dp_tiles) are whole-tile
+// work, dealt round-robin. The remaining tiles form a stream-K region: their
+// K-slab iterations, taken tile after tile, are cut into sk_ctas contiguous,
+// equal ranges, one per CTA, which evens out the last waves. A range that
+// starts inside a tile leaves a partial sum: the CTA writes it to its own
+// workspace slot and raises one flag per consumer warp. The CTA whose range
+// holds the first slab of that tile owns it: after its own slabs it adds the
+// partial sums of the following CTAs in CTA order (a fixed, deterministic
+// order) and stores the tile. Each consumer warp writes, flags, waits for and
+// reads only its own fragment, so there is no CTA-wide barrier to strand a
+// warp. The cross-CTA waits need all CTAs resident, so such launches are
+// cooperative.
+//
+// Every wait (mbarrier phase or partial-sum flag) is bounded in time (about a
+// second): on giving up, the thread sets the device error word (read by
+// sgemm_check_status()) and gives up its work; the producer first waits
+// (bounded as well) for every copy it has issued, so no copy can land in the
+// shared memory of an exited CTA.
 #include "common.cuh"
 #include "configs.cuh"
 #include "ptx.cuh"
@@ -64,17 +78,54 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
     return false;
 }
 
-template <int BM_, int BN_, int BK_, int STAGES_, bool PAIRED_, int MIN_BLOCKS_>
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag != 0; false after kWaitLimitNs.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag)
+{
+    if (ld_acquire_gpu(flag) != 0) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0; n < kSpinLimit; ++n) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) != 0) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+template <int BM_, int BN_, int BK_, int STAGES_, int TN_, bool PAIRED_, int MIN_BLOCKS_>
 struct FfmaTmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr bool PAIRED = PAIRED_;   // FFMA2 (two FP32 FMAs per instruction)
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
-    // Warp tile 64 x 32 as 8 x 4 threads, thread tile 8 x 8.
-    static constexpr int WM = 64, WN = 32, TM = 8, TN = 8;
-    static constexpr int TROWS = WM / TM, TCOLS = WN / TN;
+    // Thread tile TM x TN; warp = 8 x 4 threads, so warp tile 64 x 4*TN.
+    static constexpr int TM = 8, TN = TN_, G = TN / 4;
+    static constexpr int TROWS = 8, TCOLS = 4;
+    static constexpr int WM = TROWS * TM, WN = TCOLS * TN;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMERS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMERS + 1) * 32;
+    static constexpr int CONSUMER_THREADS = CONSUMERS * 32;
+    // Producer: one warp, or (wide thread tiles) a whole warpgroup that hands
+    // registers to the consumer warpgroups with setmaxnreg: each SM
+    // sub-partition's register file then holds 1 producer warp at
+    // PRODUCER_REGS and 2 consumer warps at CONSUMER_REGS.
+    static constexpr bool REG_SPLIT = TN > 8;
+    static constexpr int PRODUCER_WARPS = REG_SPLIT ? 4 : 1;
+    static constexpr int THREADS = CONSUMER_THREADS + 32 * PRODUCER_WARPS;
+    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
+    static constexpr int PRODUCER_REGS = 40;
+    static constexpr int CONSUMER_REGS =
+        ((LAUNCH_REGS * THREADS - PRODUCER_REGS * 32 * PRODUCER_WARPS) / CONSUMER_THREADS) / 8 * 8;
     static constexpr int A_ROW_BYTES = BK * 4;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_ROW_BYTES = BN * 4;
@@ -85,23 +136,93 @@ struct FfmaTmaCfg {
     // swz(r) = r & 7 for 128-byte rows, (r >> 1) & 3 for 64-byte rows.
     static constexpr CUtensorMapSwizzle A_SWIZZLE =
         BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    static_assert(TROWS == 8 && TCOLS == 4, "thread layout is 8 x 4 per warp");
+    static_assert(TN % 4 == 0 && TN >= 8 && TN <= 16, "thread tile columns: 8, 12 or 16");
     static_assert(BM % WM == 0 && BN % WN == 0, "block tile must hold whole warp tiles");
     static_assert(BK == 32 || BK == 16, "BK is 16 or 32");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage buffers stay 1024-aligned");
     static_assert(BN <= 256 && BM <= 256, "TMA box dimensions are at most 256");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(BM * BN == CONSUMER_THREADS * TM * TN, "one partial sum per accumulator");
+    static_assert(!REG_SPLIT || (CONSUMERS % 4 == 0 && CONSUMER_REGS <= 255), "whole consumer warpgroups");
+    // The split may not ask for more registers than the CTA was launched with.
+    static_assert(!REG_SPLIT || PRODUCER_REGS * 32 * PRODUCER_WARPS + CONSUMER_REGS * CONSUMER_THREADS <=
+                                    LAUNCH_REGS * THREADS,
+                  "register split exceeds the launch allocation");
 };
+
+// The work schedule, computed on the host (make_schedule) and read by every
+// thread. See the file comment.
+struct Schedule {
+    int tiles_m, tiles_n;
+    int nk;             // K slabs per tile
+    int grid;           // CTAs launched
+    int64_t tiles;      // all output tiles
+    int64_t dp_tiles;   // whole-tile work: tiles [0, dp_tiles), round-robin
+    int64_t sk_iters;   // slab iterations of the stream-K region
+    int sk_ctas;        // CTAs [0, sk_ctas) share those iterations
+    unsigned *flags;    // sk_ctas x CONSUMERS flags (zeroed before launch)
+    float *partials;    // sk_ctas slots of BM x BN floats
+};
+
+// One unit of work: slabs [kb0, kb1) of output tile `tile`.
+struct Item {
+    int64_t tile;
+    int kb0, kb1;
+};
+
+struct Cursor {
+    int64_t dp_next;        // next whole tile of this CTA
+    int64_t sk_pos, sk_end; // this CTA's stream-K iteration range
+};
+
+__device__ __forceinline__ int64_t sk_start(const Schedule &s, int g)
+{
+    return s.sk_iters * g / s.sk_ctas;
+}
+
+__device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
+{
+    Cursor c;
+    c.dp_next = g;
+    if (g < s.sk_ctas) {
+        c.sk_pos = sk_start(s, g);
+        c.sk_end = sk_start(s, g + 1);
+    } else {
+        c.sk_pos = c.sk_end = 0;
+    }
+    return c;
+}
+
+__device__ __forceinline__ bool next_item(const Schedule &s, Cursor &c, Item &it)
+{
+    if (c.dp_next < s.dp_tiles) {
+        it.tile = c.dp_next;
+        it.kb0 = 0;
+        it.kb1 = s.nk;
+        c.dp_next += s.grid;
+        return true;
+    }
+    if (c.sk_pos < c.sk_end) {
+        const int64_t rel = c.sk_pos / s.nk;
+        it.tile = s.dp_tiles + rel;
+        it.kb0 = (int)(c.sk_pos - rel * s.nk);
+        const int64_t left = c.sk_end - c.sk_pos;
+        it.kb1 = (int)(left < s.nk - it.kb0 ? it.kb0 + left : s.nk);
+        c.sk_pos += it.kb1 - it.kb0;
+        return true;
+    }
+    return false;
+}
 
 // Output tile of linear index t: groups of 8 block rows, column-major inside
 // a group, so the CTAs running at the same time touch few A and B panels.
 __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
 {
-    constexpr int G = 8;
-    const int64_t per_group = (int64_t)G * tiles_n;
+    constexpr int GR = 8;
+    const int64_t per_group = (int64_t)GR * tiles_n;
     const int64_t group = t / per_group;
-    const int first_m = (int)(group * G);
-    const int rows = min(tiles_m - first_m, G);
+    const int first_m = (int)(group * GR);
+    const int rows = min(tiles_m - first_m, GR);
     const int64_t local = t - group * per_group;
     tm = first_m + (int)(local % rows);
     tn = (int)(local / rows);
@@ -111,10 +232,11 @@ template <class Cfg, bool VEC_C>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapB,
-                      float *__restrict__ C, int64_t ldc, int M, int N, int K,
-                      unsigned int *status)
+                      float *__restrict__ C, int64_t ldc, int M, int N,
+                      const Schedule sched, unsigned int *status)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int TN = Cfg::TN, G = Cfg::G;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -126,9 +248,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int64_t tiles = (int64_t)tiles_m * tiles_n;
-    const int nk = (K + BK - 1) / BK;
+    const int g = blockIdx.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -139,9 +259,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     }
     __syncthreads();
 
-    if (warp == Cfg::CONSUMERS) {
+    if (warp >= Cfg::CONSUMERS) {
         // ------------------------------ producer ------------------------------
-        if (lane != 0) return;
+        if constexpr (Cfg::REG_SPLIT) ptx::setmaxnreg_dec<Cfg::PRODUCER_REGS>();
+        if (warp != Cfg::CONSUMERS || lane != 0) return;
         ptx::prefetch_tensormap(&mapA);
         ptx::prefetch_tensormap(&mapB);
         const uint64_t policy = ptx::policy_evict_last();
@@ -150,10 +271,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        Cursor cur = cursor_init(sched, g);
+        Item item;
+        while (ok && next_item(sched, cur, item)) {
             int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, tm, tn);
-            for (int kb = 0; kb < nk; ++kb, ++it) {
+            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+            for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
                 const int s = (int)(it % STAGES);
                 const int round = (int)(it / STAGES);
                 if (!wait_phase(empty_bar(s), (round & 1) ^ 1)) {
@@ -177,30 +300,36 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     }
 
     // ------------------------------ consumers ------------------------------
+    if constexpr (Cfg::REG_SPLIT) ptx::setmaxnreg_inc<Cfg::CONSUMER_REGS>();
     const int wm = (warp / Cfg::WARPS_N) * Cfg::WM;
     const int wn = (warp % Cfg::WARPS_N) * Cfg::WN;
     const int ty = lane / Cfg::TCOLS;   // 0..7: thread row (rows wm + ty + 8i)
-    const int tx = lane % Cfg::TCOLS;   // 0..3: thread column (cols wn + 4tx + 16g + e)
+    const int tx = lane % Cfg::TCOLS;   // 0..3: thread column (cols wn + 4tx + 16q + e)
     const uint32_t a_row_off = (uint32_t)(wm + ty) * Cfg::A_ROW_BYTES;
     const uint32_t a_xor = (BK == 32) ? (uint32_t)(ty & 7) : (uint32_t)((ty >> 1) & 3);
     const uint32_t b_col_off = (uint32_t)(wn + tx * 4) * 4;
+    const int ct = warp * 32 + lane;    // consumer thread index (partial-sum layout)
 
     uint32_t it = 0;
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    Cursor cur = cursor_init(sched, g);
+    Item item;
+    while (next_item(sched, cur, item)) {
         int tm, tn;
-        tile_coords(t, tiles_m, tiles_n, tm, tn);
+        tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
 
-        float acc[8][8];
-        float2 accp[8][4];
+        // acc[i][4q + e] holds C[row i][column group q, element e]; accp is
+        // the same tile as FFMA2 pairs (e = 0,1 and e = 2,3).
+        float acc[8][TN];
+        float2 accp[8][TN / 2];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) accp[i][q] = make_float2(0.0f, 0.0f);
+            for (int j = 0; j < TN / 2; ++j) accp[i][j] = make_float2(0.0f, 0.0f);
         }
 
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
             const int s = (int)(it % STAGES);
             if (!wait_phase(full_bar(s), (it / STAGES) & 1)) {
                 atomicOr(status, kStatusTimeout);
@@ -219,26 +348,28 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const int k = kg * 4 + kk;
-                    const float4 b0 = *reinterpret_cast<const float4 *>(Bs + k * Cfg::B_ROW_BYTES);
-                    const float4 b1 = *reinterpret_cast<const float4 *>(Bs + k * Cfg::B_ROW_BYTES + 64);
+                    float4 b[G];
+#pragma unroll
+                    for (int q = 0; q < G; ++q)
+                        b[q] = *reinterpret_cast<const float4 *>(Bs + k * Cfg::B_ROW_BYTES + 64 * q);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
                         if constexpr (Cfg::PAIRED) {
                             const float2 aa = make_float2(av, av);
-                            accp[i][0] = __ffma2_rn(aa, make_float2(b0.x, b0.y), accp[i][0]);
-                            accp[i][1] = __ffma2_rn(aa, make_float2(b0.z, b0.w), accp[i][1]);
-                            accp[i][2] = __ffma2_rn(aa, make_float2(b1.x, b1.y), accp[i][2]);
-                            accp[i][3] = __ffma2_rn(aa, make_float2(b1.z, b1.w), accp[i][3]);
+#pragma unroll
+                            for (int q = 0; q < G; ++q) {
+                                accp[i][2 * q] = __ffma2_rn(aa, make_float2(b[q].x, b[q].y), accp[i][2 * q]);
+                                accp[i][2 * q + 1] = __ffma2_rn(aa, make_float2(b[q].z, b[q].w), accp[i][2 * q + 1]);
+                            }
                         } else {
-                            acc[i][0] = fmaf(av, b0.x, acc[i][0]);
-                            acc[i][1] = fmaf(av, b0.y, acc[i][1]);
-                            acc[i][2] = fmaf(av, b0.z, acc[i][2]);
-                            acc[i][3] = fmaf(av, b0.w, acc[i][3]);
-                            acc[i][4] = fmaf(av, b1.x, acc[i][4]);
-                            acc[i][5] = fmaf(av, b1.y, acc[i][5]);
-                            acc[i][6] = fmaf(av, b1.z, acc[i][6]);
-                            acc[i][7] = fmaf(av, b1.w, acc[i][7]);
+#pragma unroll
+                            for (int q = 0; q < G; ++q) {
+                                acc[i][4 * q + 0] = fmaf(av, b[q].x, acc[i][4 * q + 0]);
+                                acc[i][4 * q + 1] = fmaf(av, b[q].y, acc[i][4 * q + 1]);
+                                acc[i][4 * q + 2] = fmaf(av, b[q].z, acc[i][4 * q + 2]);
+                                acc[i][4 * q + 3] = fmaf(av, b[q].w, acc[i][4 * q + 3]);
+                            }
                         }
                     }
                 }
@@ -247,16 +378,54 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             if (lane == 0) ptx::mbar_arrive(empty_bar(s));
         }
 
-        // Epilogue: rows wm+ty+8i, two runs of 4 columns per row.
         if constexpr (Cfg::PAIRED) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                acc[i][0] = accp[i][0].x; acc[i][1] = accp[i][0].y;
-                acc[i][2] = accp[i][1].x; acc[i][3] = accp[i][1].y;
-                acc[i][4] = accp[i][2].x; acc[i][5] = accp[i][2].y;
-                acc[i][6] = accp[i][3].x; acc[i][7] = accp[i][3].y;
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < TN / 2; ++j) {
+                    acc[i][2 * j] = accp[i][j].x;       // accp[i][j] = columns 2j, 2j+1
+                    acc[i][2 * j + 1] = accp[i][j].y;
+                }
+        }
+
+        if (item.kb0 > 0) {
+            // Partial sum of a tile owned by an earlier CTA: this CTA's slot,
+            // float4 v of consumer thread ct at index v * CONSUMER_THREADS + ct.
+            float4 *slot = reinterpret_cast<float4 *>(sched.partials + (int64_t)g * BM * BN);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < G; ++q)
+                    slot[(i * G + q) * Cfg::CONSUMER_THREADS + ct] =
+                        make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(sched.flags + (int64_t)g * Cfg::CONSUMERS + warp, 1u);
+            continue;
+        }
+        if (item.kb1 < sched.nk) {
+            // This CTA owns the tile: add the later CTAs' partial sums in order.
+            const int64_t tile_end = (item.tile - sched.dp_tiles + 1) * sched.nk;
+            for (int h = g + 1; h < sched.sk_ctas && sk_start(sched, h) < tile_end; ++h) {
+                if (!wait_flag(sched.flags + (int64_t)h * Cfg::CONSUMERS + warp)) {
+                    atomicOr(status, kStatusTimeout);
+                    return;
+                }
+                const float4 *slot = reinterpret_cast<const float4 *>(sched.partials + (int64_t)h * BM * BN);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int q = 0; q < G; ++q) {
+                        const float4 p = slot[(i * G + q) * Cfg::CONSUMER_THREADS + ct];
+                        acc[i][4 * q] += p.x;
+                        acc[i][4 * q + 1] += p.y;
+                        acc[i][4 * q + 2] += p.z;
+                        acc[i][4 * q + 3] += p.w;
+                    }
             }
         }
+
+        // Epilogue: rows wm+ty+8i, G runs of 4 columns per row.
         const int64_t row0 = (int64_t)tm * BM + wm + ty;
         const int col0 = tn * BN + wn + tx * 4;
 #pragma unroll
@@ -265,25 +434,27 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             if (row >= M) break;
             float *crow = C + row * ldc;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int col = col0 + 16 * g;
+            for (int q = 0; q < G; ++q) {
+                const int col = col0 + 16 * q;
                 if (VEC_C && col + 3 < N) {
                     *reinterpret_cast<float4 *>(crow + col) =
-                        make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2], acc[i][4 * g + 3]);
+                        make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (col + e < N) crow[col + e] = acc[i][4 * g + e];
+                        if (col + e < N) crow[col + e] = acc[i][4 * q + e];
                 }
             }
         }
     }
 }
 
-using CfgFfma128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, false, 1>;
-using CfgFfma2_128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, true, 1>;
-using CfgFfma2_128x128k16s8 = FfmaTmaCfg<128, 128, 16, 8, true, 1>;
-using CfgFfma2_128x64k32s4 = FfmaTmaCfg<128, 64, 32, 4, true, 2>;
+// Configurations: <BM, BN, BK, STAGES, TN, PAIRED, MIN_BLOCKS>.
+using CfgFfma128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, 8, false, 1>;
+using CfgFfma2_128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, 8, true, 1>;
+using CfgFfma2_128x128k16s8 = FfmaTmaCfg<128, 128, 16, 8, 8, true, 1>;
+using CfgFfma2_128x64k32s4 = FfmaTmaCfg<128, 64, 32, 4, 8, true, 2>;
+using CfgFfma2_128x256k32s4 = FfmaTmaCfg<128, 256, 32, 4, 16, true, 1>;
 
 std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
@@ -332,6 +503,58 @@ cudaError_t set_smem_limit()
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
 }
 
+constexpr size_t kFlagBytesAlign = 256;
+
+size_t round_up_bytes(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The schedule of a product (without workspace pointers). `with_sk` false
+// gives the whole-tile schedule.
+template <class Cfg>
+Schedule make_schedule(const GemmArgs &g, bool with_sk)
+{
+    Schedule s{};
+    s.tiles_m = (int)((g.M + Cfg::BM - 1) / Cfg::BM);
+    s.tiles_n = (int)((g.N + Cfg::BN - 1) / Cfg::BN);
+    s.nk = (int)((g.K + Cfg::BK - 1) / Cfg::BK);
+    s.tiles = (int64_t)s.tiles_m * s.tiles_n;
+    const int64_t slots = (int64_t)g.num_sms * Cfg::MIN_BLOCKS;
+    s.dp_tiles = s.tiles;
+    s.sk_iters = 0;
+    s.sk_ctas = 0;
+    s.grid = (int)(s.tiles < slots ? s.tiles : slots);
+    bool sk = false;
+    if (with_sk && g.sched == kSchedStreamK) {
+        sk = true;
+    } else if (with_sk && g.sched == kSchedAuto) {
+        // Stream-K only when whole tiles would leave the last wave short:
+        // efficiency = tiles / (rounds * slots) below 97%.
+        const int64_t rounds = (s.tiles + slots - 1) / slots;
+        sk = (double)s.tiles < 0.97 * (double)(rounds * slots) && s.nk >= 8;
+    }
+    if (!sk) return s;
+    const int64_t full_rounds = s.tiles / slots;
+    const int64_t dp_rounds = (g.sched == kSchedStreamK || full_rounds < 1) ? 0 : full_rounds - 1;
+    s.dp_tiles = dp_rounds * slots;
+    s.sk_iters = (s.tiles - s.dp_tiles) * s.nk;
+    // Forced stream-K splits as finely as one slab per CTA (to exercise the
+    // fix-up path); the automatic choice keeps at least 4 slabs per CTA.
+    const int64_t min_iters = g.sched == kSchedStreamK ? 1 : 4;
+    int64_t ctas = s.sk_iters / min_iters;
+    if (ctas > slots) ctas = slots;
+    if (ctas < 1) ctas = 1;
+    s.sk_ctas = (int)ctas;
+    s.grid = (int)(s.dp_tiles > 0 ? slots : ctas);
+    return s;
+}
+
+template <class Cfg>
+size_t workspace_bytes(const Schedule &s)
+{
+    if (s.sk_ctas == 0) return 0;
+    return round_up_bytes((size_t)s.sk_ctas * Cfg::CONSUMERS * sizeof(unsigned), kFlagBytesAlign) +
+           (size_t)s.sk_ctas * Cfg::BM * Cfg::BN * sizeof(float);
+}
+
 template <class Cfg>
 cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
 {
@@ -340,16 +563,32 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     e = encode_2d(&mapB, g.B, g.K, g.N, g.ldb, Cfg::BK, Cfg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = ((g.M + Cfg::BM - 1) / Cfg::BM) * ((g.N + Cfg::BN - 1) / Cfg::BN);
-    const int64_t slots = (int64_t)g.num_sms * Cfg::MIN_BLOCKS;
-    const unsigned grid = (unsigned)(tiles < slots ? tiles : slots);
+    // Stream-K needs the caller's workspace; without one the schedule is whole tiles.
+    Schedule s = make_schedule<Cfg>(g, g.workspace != nullptr);
+    if (s.sk_ctas > 0 && g.workspace_bytes < workspace_bytes<Cfg>(s)) s = make_schedule<Cfg>(g, false);
+    if (s.sk_ctas > 0) {
+        const size_t flag_bytes =
+            round_up_bytes((size_t)s.sk_ctas * Cfg::CONSUMERS * sizeof(unsigned), kFlagBytesAlign);
+        s.flags = static_cast<unsigned *>(g.workspace);
+        s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(g.workspace) + flag_bytes);
+        e = cudaMemsetAsync(s.flags, 0, flag_bytes, stream);
+        if (e != cudaSuccess) return e;
+    }
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
-    if (vec)
-        sgemm_ffma_tma_kernel<Cfg, true><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
-            mapA, mapB, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+    float *C = g.C;
+    int64_t ldc = g.ldc;
+    int M = (int)g.M, N = (int)g.N;
+    unsigned int *status = g.status;
+    void *args[] = {&mapA, &mapB, &C, &ldc, &M, &N, &s, &status};
+    const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true>)
+                         : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false>);
+    // Owners wait on other CTAs' partial sums: all CTAs must be resident.
+    const bool coop = s.sk_ctas > 1;
+    if (coop)
+        e = cudaLaunchCooperativeKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
     else
-        sgemm_ffma_tma_kernel<Cfg, false><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
-            mapA, mapB, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+        e = cudaLaunchKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -363,16 +602,30 @@ cudaError_t prepare_ffma_tma()
     if ((e = set_smem_limit<CfgFfma128x128k32s4>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x128k32s4>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x128k16s8>()) != cudaSuccess) return e;
-    return set_smem_limit<CfgFfma2_128x64k32s4>();
+    if ((e = set_smem_limit<CfgFfma2_128x64k32s4>()) != cudaSuccess) return e;
+    return set_smem_limit<CfgFfma2_128x256k32s4>();
 }
 
-cudaError_t launch_ffma_tma(int cfg, const GemmArgs &g, cudaStream_t stream)
+size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
 {
-    switch (cfg) {
-    case kCfgFfma128x128k32s4: return launch<CfgFfma128x128k32s4>(g, stream);
-    case kCfgFfma2_128x128k32s4: return launch<CfgFfma2_128x128k32s4>(g, stream);
-    case kCfgFfma2_128x128k16s8: return launch<CfgFfma2_128x128k16s8>(g, stream);
-    case kCfgFfma2_128x64k32s4: return launch<CfgFfma2_128x64k32s4>(g, stream);
+    switch (kernel) {
+    case kKernFfma128x128k32s4: return workspace_bytes<CfgFfma128x128k32s4>(make_schedule<CfgFfma128x128k32s4>(g, true));
+    case kKernFfma2_128x128k32s4: return workspace_bytes<CfgFfma2_128x128k32s4>(make_schedule<CfgFfma2_128x128k32s4>(g, true));
+    case kKernFfma2_128x128k16s8: return workspace_bytes<CfgFfma2_128x128k16s8>(make_schedule<CfgFfma2_128x128k16s8>(g, true));
+    case kKernFfma2_128x64k32s4: return workspace_bytes<CfgFfma2_128x64k32s4>(make_schedule<CfgFfma2_128x64k32s4>(g, true));
+    case kKernFfma2_128x256k32s4: return workspace_bytes<CfgFfma2_128x256k32s4>(make_schedule<CfgFfma2_128x256k32s4>(g, true));
+    default: return 0;
+    }
+}
+
+cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
+{
+    switch (kernel) {
+    case kKernFfma128x128k32s4: return launch<CfgFfma128x128k32s4>(g, stream);
+    case kKernFfma2_128x128k32s4: return launch<CfgFfma2_128x128k32s4>(g, stream);
+    case kKernFfma2_128x128k16s8: return launch<CfgFfma2_128x128k16s8>(g, stream);
+    case kKernFfma2_128x64k32s4: return launch<CfgFfma2_128x64k32s4>(g, stream);
+    case kKernFfma2_128x256k32s4: return launch<CfgFfma2_128x256k32s4>(g, stream);
     default: return cudaErrorInvalidValue;
     }
 }

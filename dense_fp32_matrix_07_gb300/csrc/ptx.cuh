@@ -52,17 +52,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// Waits for the phase with the given parity to complete, giving up after
-// `limit` probes (each probe may itself suspend the thread for a while).
-// Returns false on giving up; the caller records the timeout and unwinds.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit)
+// Register reallocation between the warpgroups of a CTA (all 128 threads of
+// a warpgroup execute the same instruction).
+template <int REGS>
+__device__ __forceinline__ void setmaxnreg_dec()
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    for (uint32_t n = 0; n < limit; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (n > 64) __nanosleep(128);
-    }
-    return false;
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS));
+}
+
+template <int REGS>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS));
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)

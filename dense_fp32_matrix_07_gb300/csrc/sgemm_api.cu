@@ -204,42 +204,53 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
 
     GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
-    float *scratch = nullptr;
-    if (kConfigTable[cfg].uses_tma) {
-        const bool pa = needs_pack(a, lda), pb = needs_pack(b, ldb);
-        // Packed rows are padded to a multiple of 32 floats (128 bytes).
-        const int64_t lda_p = round_up(K, 32), ldb_p = round_up(N, 32);
-        const int64_t elems = (pa ? M * lda_p : 0) + (pb ? K * ldb_p : 0);
-        if (elems > 0) {
-            if (cudaMallocFromPoolAsync((void **)&scratch, (size_t)elems * 4, dev->pool,
-                                        stream) != cudaSuccess) {
-                cudaGetLastError();
-                return SGEMM_ERR_ALLOC;
+    g.sched = kConfigTable[cfg].sched;
+    // One scratch allocation, carved into: packed A, packed B (rows padded to
+    // a multiple of 32 floats = 128 bytes), then the stream-K workspace.
+    const bool tma = kConfigTable[cfg].uses_tma;
+    const bool pa = tma && needs_pack(a, lda), pb = tma && needs_pack(b, ldb);
+    const int64_t lda_p = round_up(K, 32), ldb_p = round_up(N, 32);
+    const size_t a_bytes = pa ? (size_t)(M * lda_p) * 4 : 0;
+    const size_t b_bytes = pb ? (size_t)(K * ldb_p) * 4 : 0;
+    const size_t ws_off = (a_bytes + b_bytes + 255) / 256 * 256;
+    const size_t ws_bytes = config_workspace_bytes(cfg, g);
+    const size_t total = ws_off + ws_bytes;
+    uint8_t *scratch = nullptr;
+    if (total > 0) {
+        if (cudaMallocFromPoolAsync((void **)&scratch, total, dev->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_ALLOC;
+        }
+        if (pa) {
+            float *dst = reinterpret_cast<float *>(scratch);
+            if (launch_pack(A, M, K, lda, dst, lda_p, stream) != cudaSuccess) {
+                cudaFreeAsync(scratch, stream);
+                return SGEMM_ERR_LAUNCH;
             }
-            float *next = scratch;
-            if (pa) {
-                if (launch_pack(A, M, K, lda, next, lda_p, stream) != cudaSuccess) {
-                    cudaFreeAsync(scratch, stream);
-                    return SGEMM_ERR_LAUNCH;
-                }
-                g.A = next;
-                g.lda = lda_p;
-                next += M * lda_p;
+            g.A = dst;
+            g.lda = lda_p;
+        }
+        if (pb) {
+            float *dst = reinterpret_cast<float *>(scratch + a_bytes);
+            if (launch_pack(B, K, N, ldb, dst, ldb_p, stream) != cudaSuccess) {
+                cudaFreeAsync(scratch, stream);
+                return SGEMM_ERR_LAUNCH;
             }
-            if (pb) {
-                if (launch_pack(B, K, N, ldb, next, ldb_p, stream) != cudaSuccess) {
-                    cudaFreeAsync(scratch, stream);
-                    return SGEMM_ERR_LAUNCH;
-                }
-                g.B = next;
-                g.ldb = ldb_p;
-            }
+            g.B = dst;
+            g.ldb = ldb_p;
+        }
+        if (ws_bytes > 0) {
+            g.workspace = scratch + ws_off;
+            g.workspace_bytes = ws_bytes;
         }
     }
 
     const cudaError_t err = launch_config(cfg, g, stream);
     if (scratch) cudaFreeAsync(scratch, stream);
-    if (err != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
     return SGEMM_OK;
 }
 

@@ -162,6 +162,7 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         return SGEMM_ERR_SCRATCH_LIMIT;
 
     GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
+    g.sched = kSchedDataParallel;   // whole tiles: no stream-K workspace needed
     if (pack_a) {
         if (pack_into_scratch(A, M, K, lda, 0, lda_p, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         g.A = dev->scratch;
