@@ -12,7 +12,9 @@ data path): scaling is weak.
 
 Also reported on the same JSON line:
   e2e           the same metric through the same call with host buffers:
-                pinned host A, B copied in, C copied out, inside the timing;
+                pinned host A, B copied in, C copied out, inside the timing
+                (steps pipelined over two buffer sets and three streams; the
+                serial figure is reported beside it);
   roofline      the main kernel's achieved FP32 FLOP/s (CUDA events on its
                 stream) against the FFMA peak SMs x 128 lanes x 2 FLOP x max
                 SM clock ("alu"-bound: the intensity is far above the HBM
@@ -49,6 +51,40 @@ L2_BYTES = 126.5 * 2 ** 20       # GB300 L2 capacity
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffma_tma_sq4096.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_07_gb300", "csrc", f)
                   for f in ("kernels_ffma_tma.cu", "ptx.cuh")]
+
+
+def product_flops(M: int, N: int, K: int) -> float:
+    """2MNK: one multiply and one add per term of every output's dot product
+    (Chapter 9: Optimised Matrix Multiplication, section 9.1: 2N^3 for N x N)."""
+    return 2.0 * M * N * K
+
+
+def compulsory_bytes(M: int, N: int, K: int) -> float:
+    """4(MK + KN + MN): each FP32 element of A and B read once, C written once
+    (section 9.1 counts 3N^2 elements, 12N^2 bytes, for N x N)."""
+    return 4.0 * (M * K + K * N + M * N)
+
+
+def intensity(M: int, N: int, K: int) -> float:
+    """Arithmetic intensity in FLOP/byte (section 9.1: N/6 for N x N)."""
+    return product_flops(M, N, K) / compulsory_bytes(M, N, K)
+
+
+def max_over_ranks(values, dist_mod=None, device="cpu"):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's
+    times); the values themselves when there is no process group."""
+    if dist_mod is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gflops(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank ran `steps` products in at most
+    `seconds` (weak scaling: each rank has its own problem)."""
+    return flops_per_step * steps * world / seconds / 1e9
 
 
 def kernel_source_hash() -> str:
@@ -125,40 +161,47 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            # timestamp, index, clocks.sm, clocks.max.sm, power.draw, active,
-            # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
-            if len(parts) < 10:
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
-                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
-                             "sw_power": parts[9]})
-            except ValueError:
-                continue
+        with open(self.path) as f:
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        # Samples taken inside the timed region (host and nvidia-smi share the
-        # clock); if the region was shorter than the sampling period, the
-        # samples nearest to it.
-        inside = [r for r in rows if self.t_start - 0.03 <= r["t"] <= self.t_end + 0.03]
-        if not inside:
-            mid = 0.5 * (self.t_start + self.t_end)
-            inside = sorted(rows, key=lambda r: abs(r["t"] - mid))[:2]
-        load = inside
-        reasons = set()
-        for r in load:
-            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
-                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
-                if r[key].lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in load),
-                "sm_max_mhz": max(r["max"] for r in load),
-                "samples": len(load), "reasons": sorted(reasons)}
+        return parse_clock_samples(lines, self.t_start, self.t_end)
+
+
+def parse_clock_samples(lines, t_start, t_end):
+    """Summary of nvidia-smi CSV samples (the ClockSampler query fields):
+    median SM clock and max SM clock over the samples inside [t_start,
+    t_end] (host and nvidia-smi share the wall clock), plus every throttle
+    reason seen active; the two samples nearest the window when the window
+    was shorter than the sampling period; None without samples."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        # timestamp, index, clocks.sm, clocks.max.sm, power.draw, active,
+        # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append({"t": ts, "sm": float(parts[2]), "max": float(parts[3]),
+                         "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                         "sw_power": parts[9]})
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    inside = [r for r in rows if t_start - 0.03 <= r["t"] <= t_end + 0.03]
+    if not inside:
+        mid = 0.5 * (t_start + t_end)
+        inside = sorted(rows, key=lambda r: abs(r["t"] - mid))[:2]
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+            "sm_max_mhz": max(r["max"] for r in inside),
+            "samples": len(inside), "reasons": sorted(reasons)}
 
 
 def nvsmi_gpu_id(dev, local: int) -> str:
@@ -211,8 +254,7 @@ def run_reference(args, world, rank):
         oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb,
                           np.sort(rng.choice(w.M, rows_per_step, replace=False)), want_abs=False)
     elapsed = time.perf_counter() - t0
-    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
-    value = flops / elapsed / 1e9
+    value = job_gflops(product_flops(rows_per_step, w.N, w.K), args.steps, 1, elapsed)
     sample = f"{rows_per_step} random full rows of C per step ({rows_per_step}x{w.N}x{w.K})"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s",
@@ -257,7 +299,7 @@ def cpu_baseline(w, A, B):
     t0 = time.perf_counter()
     oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, rows, want_abs=False)
     dt = time.perf_counter() - t0
-    return {"value": round(2.0 * len(rows) * w.N * w.K / dt / 1e9, 3), "unit": "GFLOP/s",
+    return {"value": round(job_gflops(product_flops(len(rows), w.N, w.K), 1, 1, dt), 3), "unit": "GFLOP/s",
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(rows)} sampled full rows of C ({len(rows)}x{w.N}x{w.K}), {dt:.1f} s"}
 
@@ -270,7 +312,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="sq4096", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--config", type=int, default=-1, help="force a kernel config id")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -308,7 +350,7 @@ def main():
         cfg = args.config
     cfg_name = sg.sgemm_config_name(cfg)
     launches_per_step = 1 + pa + pb
-    flops = 2.0 * w.M * w.N * w.K
+    flops = product_flops(w.M, w.N, w.K)
 
     total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
     flush = None
@@ -354,41 +396,86 @@ def main():
     if sg.sgemm_check_status(sh) != 0:
         raise RuntimeError("device status after the timed region")
 
-    t_max = step_s
-    if pg is not None:
-        t = torch.tensor([step_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = flops * args.steps * world / t_max / 1e9
+    (t_max,) = max_over_ranks([step_s], pg, dev)
+    value = job_gflops(flops, args.steps, world, t_max)
 
     # ---- e2e: host buffers, copies inside the timing ----
+    # Every step copies A and B in from pinned host memory, runs the product
+    # through the C ABI and copies C back. "serial" does the three in order
+    # on one stream; "pipelined" is how a caller streams independent steps:
+    # two buffer sets and three streams, so the copies of one step overlap
+    # the product of another.
     hA = A.pin_memory()
     hB = B.pin_memory()
-    hC = torch.empty((w.M, w.ldc), dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    hC = [torch.empty((w.M, w.ldc), dtype=torch.float32).pin_memory() for _ in range(2)]
+    e2e_steps = max(2, min(args.e2e_steps, args.steps))
+    dA2, dB2 = torch.empty_like(dA), torch.empty_like(dB)
+    dC2 = torch.empty_like(dC)
+    sets = [(dA, dB, dC), (dA2, dB2, dC2)]
 
-    def e2e_step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        step()
-        hC.copy_(dC, non_blocking=True)
+    def product(a, b, c, stream_handle):
+        r = sg.sgemm_ex(w.M, w.N, w.K, a.data_ptr(), w.lda, b.data_ptr(), w.ldb,
+                        c.data_ptr(), w.ldc, args.config, stream_handle)
+        if r != 0:
+            raise RuntimeError(sg.sgemm_error_string(r))
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_serial(n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            product(dA, dB, dC, sh)
+            hC[0].copy_(dC, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3
+
+    s_in, s_mm, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def e2e_pipelined(n):
+        done_in = [torch.cuda.Event() for _ in range(2)]
+        done_mm = [torch.cuda.Event() for _ in range(2)]
+        done_out = [torch.cuda.Event() for _ in range(2)]
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for s_ in (s_in, s_mm, s_out):
+            s_.wait_event(ev0)
+        for i in range(n):
+            k = i % 2
+            a, b, c = sets[k]
+            if i >= 2:
+                s_in.wait_event(done_mm[k])      # the product reading a, b is done
+            with torch.cuda.stream(s_in):
+                a.copy_(hA, non_blocking=True)
+                b.copy_(hB, non_blocking=True)
+            done_in[k].record(s_in)
+            s_mm.wait_event(done_in[k])
+            if i >= 2:
+                s_mm.wait_event(done_out[k])     # C of two steps ago has been read
+            product(a, b, c, s_mm.cuda_stream)
+            done_mm[k].record(s_mm)
+            s_out.wait_event(done_mm[k])
+            with torch.cuda.stream(s_out):
+                hC[k].copy_(c, non_blocking=True)
+            done_out[k].record(s_out)
+        stream.wait_stream(s_out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3
+
+    e2e_serial(2)
+    e2e_pipelined(2)
     torch.cuda.synchronize()
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = ev0.elapsed_time(ev1) / 1e3
-    if pg is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = flops * e2e_steps * world / e2e_s / 1e9
+    serial_s = e2e_serial(e2e_steps)
+    barrier()
+    e2e_s = e2e_pipelined(e2e_steps)
+    if sg.sgemm_check_status(sh) != 0:
+        raise RuntimeError("device status after the e2e steps")
+    e2e_s, serial_s = max_over_ranks([e2e_s, serial_s], pg, dev)
+    e2e_value = job_gflops(flops, e2e_steps, world, e2e_s)
+    serial_value = job_gflops(flops, e2e_steps, world, serial_s)
 
     if rank != 0:
         if pg is not None:
@@ -417,7 +504,10 @@ def main():
         "fp32_peak_pct": round(100.0 * value / world / 1e3 / peak_tflops, 2),
         "e2e": {"value": round(e2e_value, 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
-                "d2h_bytes_per_step": int(hC.numel() * 4)},
+                "d2h_bytes_per_step": int(hC[0].numel() * 4),
+                "steps": e2e_steps,
+                "mode": "pipelined: 2 buffer sets, H2D / product / D2H on 3 streams",
+                "serial_value": round(serial_value, 1)},
         "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": "alu", "achieved": round(achieved_tflops, 3),
                      "peak": round(peak_tflops, 3), "unit": "TFLOP/s",

@@ -30,7 +30,8 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
-            "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc")
+            "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
+            "sgemm_test_withhold_copy")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +60,9 @@ def load(rebuild: bool = False):
                                      ctypes.c_int, _vp]
             lib.sgemm_noalloc.restype = ctypes.c_int
             lib.sgemm_noalloc.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+            lib.sgemm_test_withhold_copy.restype = ctypes.c_int
+            lib.sgemm_test_withhold_copy.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                                     _i64, ctypes.c_int, _vp]
             lib.sgemm_check_status.restype = ctypes.c_int
             lib.sgemm_check_status.argtypes = [_vp]
             lib.sgemm_error_string.restype = ctypes.c_char_p
@@ -99,6 +103,13 @@ def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     fit. All calls on a device share that array, so calls that overlap on
     the GPU race on it."""
     return load().sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) -> int:
+    """Test hook: sgemm() whose first CTA never issues the copy of its
+    `slab`-th K slab, so the kernel's bounded waits expire (about a second)
+    and sgemm_check_status() reports SGEMM_ERR_TIMEOUT."""
+    return load().sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream)
 
 
 def sgemm_check_status(stream=0) -> int:

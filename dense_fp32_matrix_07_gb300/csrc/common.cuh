@@ -27,6 +27,7 @@ struct GemmArgs {
     int sched = kSchedDataParallel;
     void *workspace = nullptr;     // stream-K partial sums and flags, or null
     size_t workspace_bytes = 0;
+    int withhold_it = -1;          // test hook: CTA 0's producer skips this copy
 };
 
 // Bits of the device error word.

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapB,
                       float *__restrict__ C, int64_t ldc, int M, int N,
-                      const Schedule sched, unsigned int *status)
+                      const Schedule sched, unsigned int *status, int withhold_it)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TN = Cfg::TN, G = Cfg::G;
@@ -284,6 +284,9 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                     ok = false;
                     break;
                 }
+                // Test hook (sgemm_test_withhold_copy): this copy is never
+                // issued, so the consumers' wait for it must time out.
+                if (g == 0 && (int)it == withhold_it) continue;
                 ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
                 ptx::tma_load_2d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), kb * BK, tm * BM, policy);
                 ptx::tma_load_2d(sB + s * Cfg::B_BYTES, &mapB, full_bar(s), tn * BN, kb * BK, policy);
@@ -579,7 +582,8 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     int64_t ldc = g.ldc;
     int M = (int)g.M, N = (int)g.N;
     unsigned int *status = g.status;
-    void *args[] = {&mapA, &mapB, &C, &ldc, &M, &N, &s, &status};
+    int withhold = g.withhold_it;
+    void *args[] = {&mapA, &mapB, &C, &ldc, &M, &N, &s, &status, &withhold};
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false>);
     // Owners wait on other CTAs' partial sums: all CTAs must be resident.

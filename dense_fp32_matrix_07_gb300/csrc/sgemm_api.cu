@@ -172,9 +172,15 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_
     return SGEMM_OK;
 }
 
-int sgemm_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
-             const float *B, int64_t ldb, float *C, int64_t ldc, int config,
-             cudaStream_t stream)
+}  // extern "C"
+
+namespace sgemm_gb300 {
+
+// sgemm_ex() with two test-only knobs: a forced schedule policy (-1: the
+// configuration's own) and a copy for CTA 0's producer to withhold (-1: none).
+static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, int config,
+                      int sched_override, int withhold_it, cudaStream_t stream)
 {
     if (config < -1 || config >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
     int rc = check_sizes(M, N, K, lda, ldb, ldc);
@@ -204,7 +210,8 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
 
     GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
-    g.sched = kConfigTable[cfg].sched;
+    g.sched = sched_override >= 0 ? sched_override : kConfigTable[cfg].sched;
+    g.withhold_it = withhold_it;
     // One scratch allocation, carved into: packed A, packed B (rows padded to
     // a multiple of 32 floats = 128 bytes), then the stream-K workspace.
     const bool tma = kConfigTable[cfg].uses_tma;
@@ -254,10 +261,30 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     return SGEMM_OK;
 }
 
+}  // namespace sgemm_gb300
+
+extern "C" {
+
+int sgemm_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+             const float *B, int64_t ldb, float *C, int64_t ldc, int config,
+             cudaStream_t stream)
+{
+    return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, config, -1, -1, stream);
+}
+
 int sgemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
           const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream)
 {
-    return sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, -1, stream);
+    return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, -1, -1, stream);
+}
+
+int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                             const float *B, int64_t ldb, float *C, int64_t ldc, int slab,
+                             cudaStream_t stream)
+{
+    // Whole tiles: no stream-K waits between CTAs, only the withheld copy.
+    return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, kSchedDataParallel,
+                      slab < 0 ? -1 : slab, stream);
 }
 
 int sgemm_check_status(cudaStream_t stream)

@@ -148,6 +148,27 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K,
                int *out_config, int *out_pack_a, int *out_pack_b);
 
 /*
+ * sgemm_test_withhold_copy — test hook for the device-side wait limit.
+ *
+ * Failure detection ("Перемножение матриц: наивное и тайловое", section 2:
+ * a tile may be used only once it is fully loaded; here that wait is
+ * bounded). Runs sgemm() with whole-tile scheduling, except that the producer
+ * of the first CTA never issues the copy of its `slab`-th K slab, so the
+ * consumers' wait for it can never be satisfied. Every device-side wait gives
+ * up after about a second; the kernel then sets the device error word and
+ * exits without faulting, the context stays usable, and sgemm_check_status()
+ * returns SGEMM_ERR_TIMEOUT. C is left incomplete. The call takes about one
+ * to two seconds on the GPU. slab < 0 behaves like sgemm() (whole tiles).
+ * Arguments otherwise as sgemm(); aligned operands make the kernel read A and
+ * B in place (no packing) so the withheld copy is the product's own.
+ */
+int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K,
+                             const float *A, int64_t lda,
+                             const float *B, int64_t ldb,
+                             float *C, int64_t ldc,
+                             int slab, cudaStream_t stream);
+
+/*
  * sgemm_noalloc — sgemm() for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for users of
