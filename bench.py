@@ -314,6 +314,7 @@ def main():
     ap.add_argument("--config", type=int, default=-1, help="force a kernel config id")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs (config sweeps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -405,13 +406,14 @@ def main():
     # on one stream; "pipelined" is how a caller streams independent steps:
     # two buffer sets and three streams, so the copies of one step overlap
     # the product of another.
-    hA = A.pin_memory()
-    hB = B.pin_memory()
-    hC = [torch.empty((w.M, w.ldc), dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(2, min(args.e2e_steps, args.steps))
-    dA2, dB2 = torch.empty_like(dA), torch.empty_like(dB)
-    dC2 = torch.empty_like(dC)
-    sets = [(dA, dB, dC), (dA2, dB2, dC2)]
+    if not args.no_e2e:
+        hA = A.pin_memory()
+        hB = B.pin_memory()
+        hC = [torch.empty((w.M, w.ldc), dtype=torch.float32).pin_memory() for _ in range(2)]
+        dA2, dB2 = torch.empty_like(dA), torch.empty_like(dB)
+        dC2 = torch.empty_like(dC)
+        sets = [(dA, dB, dC), (dA2, dB2, dC2)]
 
     def product(a, b, c, stream_handle):
         r = sg.sgemm_ex(w.M, w.N, w.K, a.data_ptr(), w.lda, b.data_ptr(), w.ldb,
@@ -464,18 +466,20 @@ def main():
         torch.cuda.synchronize()
         return ev0.elapsed_time(ev1) / 1e3
 
-    e2e_serial(2)
-    e2e_pipelined(2)
-    torch.cuda.synchronize()
-    barrier()
-    serial_s = e2e_serial(e2e_steps)
-    barrier()
-    e2e_s = e2e_pipelined(e2e_steps)
-    if sg.sgemm_check_status(sh) != 0:
-        raise RuntimeError("device status after the e2e steps")
-    e2e_s, serial_s = max_over_ranks([e2e_s, serial_s], pg, dev)
-    e2e_value = job_gflops(flops, e2e_steps, world, e2e_s)
-    serial_value = job_gflops(flops, e2e_steps, world, serial_s)
+    e2e_value = serial_value = None
+    if not args.no_e2e:
+        e2e_serial(2)
+        e2e_pipelined(2)
+        torch.cuda.synchronize()
+        barrier()
+        serial_s = e2e_serial(e2e_steps)
+        barrier()
+        e2e_s = e2e_pipelined(e2e_steps)
+        if sg.sgemm_check_status(sh) != 0:
+            raise RuntimeError("device status after the e2e steps")
+        e2e_s, serial_s = max_over_ranks([e2e_s, serial_s], pg, dev)
+        e2e_value = job_gflops(flops, e2e_steps, world, e2e_s)
+        serial_value = job_gflops(flops, e2e_steps, world, serial_s)
 
     if rank != 0:
         if pg is not None:
@@ -502,7 +506,7 @@ def main():
         "data": "synthetic",
         "config": workload_config(w, cfg_name),
         "fp32_peak_pct": round(100.0 * value / world / 1e3 / peak_tflops, 2),
-        "e2e": {"value": round(e2e_value, 1), "unit": "GFLOP/s",
+        "e2e": None if e2e_value is None else {"value": round(e2e_value, 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
                 "d2h_bytes_per_step": int(hC[0].numel() * 4),
                 "steps": e2e_steps,

@@ -14,11 +14,19 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"ffma2_128x128_k32_s4_sk", kKernFfma2_128x128k32s4, kSchedStreamK, true, 128, 128},
     {"ffma2_128x256_k32_s4_dp", kKernFfma2_128x256k32s4, kSchedDataParallel, true, 128, 256},
     {"ffma2_128x256_k32_s4_sk", kKernFfma2_128x256k32s4, kSchedStreamK, true, 128, 256},
+    {"ladder_naive_rowmap", kKernLadderNaive, kSchedDataParallel, false, 16, 16},
+    {"ladder_coalesced", kKernLadderCoalesced, kSchedDataParallel, false, 16, 16},
+    {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, 128, 128},
+    {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, 16, 16},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
 {
     if (cfg < 0 || cfg >= kNumConfigs) return false;
+    // One thread per output on a 2-D grid: grid.y (<= 65535 blocks of 16)
+    // runs over columns (row-mapped kernel) or rows (coalesced kernel).
+    if (kConfigTable[cfg].kernel == kKernLadderNaive) return p.N <= 65535 * 16;
+    if (kConfigTable[cfg].kernel == kKernLadderCoalesced) return p.M <= 65535 * 16;
     if (!kConfigTable[cfg].uses_tma) return true;
     // TMA sizes are 32-bit coordinates; strides of packed operands are at
     // most (kMaxDim rounded up) * 4 bytes, within the 2^40-byte stride limit.
@@ -50,7 +58,9 @@ size_t config_workspace_bytes(int cfg, const GemmArgs &g)
 
 cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
-    if (kConfigTable[cfg].kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
+    const int kernel = kConfigTable[cfg].kernel;
+    if (kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
+    if (kernel >= kKernLadderNaive) return launch_ladder(kernel, g, stream);
     GemmArgs a = g;
     if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
     return launch_ffma_tma(kConfigTable[cfg].kernel, a, stream);

@@ -24,6 +24,11 @@ enum KernelId : int {
     kKernFfma2_128x128k16s8,    // 128x128 block, BK 16, 8 stages, FFMA2
     kKernFfma2_128x64k32s4,     // 128x64 block (4 consumer warps), 2 CTAs per SM
     kKernFfma2_128x256k32s4,    // 128x256 block, 8x16 thread tiles, FFMA2
+    // The pages' kernel ladder (kernels_ladder.cu), for measurement.
+    kKernLadderNaive,           // one thread per output, threadIdx.x -> row
+    kKernLadderCoalesced,       // one thread per output, threadIdx.x -> column
+    kKernLadderCacheBlocked8x8, // 8x8 register micro-tiles, caches only
+    kKernLadderRegisterTiled2x2 // 16x16 padded smem tiles, 2x2 per thread
 };
 
 // Configurations = kernel instance + schedule policy.
@@ -38,6 +43,10 @@ enum ConfigId : int {
     kCfgFfma2_128x128_sk,
     kCfgFfma2_128x256_dp,
     kCfgFfma2_128x256_sk,
+    kCfgLadderNaive,
+    kCfgLadderCoalesced,
+    kCfgLadderCacheBlocked8x8,
+    kCfgLadderRegisterTiled2x2,
     kNumConfigs
 };
 
@@ -72,5 +81,8 @@ cudaError_t configs_prepare_device();
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream);
 size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g);
 cudaError_t prepare_ffma_tma();
+
+// Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
+cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);
 
 }  // namespace sgemm_gb300
