@@ -4,20 +4,21 @@
 namespace sgemm_gb300 {
 
 const ConfigInfo kConfigTable[kNumConfigs] = {
-    {"tiled16_simple", kKernTiledSimple, kSchedDataParallel, false, 16, 16},
-    {"ffma_128x128_k32_s4", kKernFfma128x128k32s4, kSchedAuto, true, 128, 128},
-    {"ffma2_128x128_k32_s4", kKernFfma2_128x128k32s4, kSchedAuto, true, 128, 128},
-    {"ffma2_128x128_k16_s8", kKernFfma2_128x128k16s8, kSchedAuto, true, 128, 128},
-    {"ffma2_128x64_k32_s4", kKernFfma2_128x64k32s4, kSchedAuto, true, 128, 64},
-    {"ffma2_128x256_k32_s4", kKernFfma2_128x256k32s4, kSchedAuto, true, 128, 256},
-    {"ffma2_128x128_k32_s4_dp", kKernFfma2_128x128k32s4, kSchedDataParallel, true, 128, 128},
-    {"ffma2_128x128_k32_s4_sk", kKernFfma2_128x128k32s4, kSchedStreamK, true, 128, 128},
-    {"ffma2_128x256_k32_s4_dp", kKernFfma2_128x256k32s4, kSchedDataParallel, true, 128, 256},
-    {"ffma2_128x256_k32_s4_sk", kKernFfma2_128x256k32s4, kSchedStreamK, true, 128, 256},
-    {"ladder_naive_rowmap", kKernLadderNaive, kSchedDataParallel, false, 16, 16},
-    {"ladder_coalesced", kKernLadderCoalesced, kSchedDataParallel, false, 16, 16},
-    {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, 128, 128},
-    {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, 16, 16},
+    {"tiled16_simple", kKernTiledSimple, kSchedDataParallel, false, false, 16, 16},
+    {"ffma_128x128_k32_s4", kKernFfma128x128k32s4, kSchedAuto, true, true, 128, 128},
+    {"ffma2_128x128_k32_s4", kKernFfma2_128x128k32s4, kSchedAuto, true, true, 128, 128},
+    {"ffma2_128x128_k16_s8", kKernFfma2_128x128k16s8, kSchedAuto, true, true, 128, 128},
+    {"ffma2_128x64_k32_s4", kKernFfma2_128x64k32s4, kSchedAuto, true, true, 128, 64},
+    {"ffma2_128x256_k32_s4", kKernFfma2_128x256k32s4, kSchedAuto, true, true, 128, 256},
+    {"ffma2_128x128_k32_s4_dp", kKernFfma2_128x128k32s4, kSchedDataParallel, true, true, 128, 128},
+    {"ffma2_128x128_k32_s4_sk", kKernFfma2_128x128k32s4, kSchedStreamK, true, true, 128, 128},
+    {"ffma2_128x256_k32_s4_dp", kKernFfma2_128x256k32s4, kSchedDataParallel, true, true, 128, 256},
+    {"ffma2_128x256_k32_s4_sk", kKernFfma2_128x256k32s4, kSchedStreamK, true, true, 128, 256},
+    {"ladder_naive_rowmap", kKernLadderNaive, kSchedDataParallel, false, false, 16, 16},
+    {"ladder_coalesced", kKernLadderCoalesced, kSchedDataParallel, false, false, 16, 16},
+    {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, false, 128, 128},
+    {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, false, 16, 16},
+    {"tf32x3_128x256_k16_s4", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
@@ -51,6 +52,7 @@ int select_config(const ProblemShape &p)
 size_t config_workspace_bytes(int cfg, const GemmArgs &g)
 {
     if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].uses_tma) return 0;
+    if (kConfigTable[cfg].kernel == kKernTf32x3_128x256) return tf32x3_workspace_bytes(g);
     GemmArgs a = g;
     a.sched = kConfigTable[cfg].sched;
     return ffma_tma_workspace_bytes(kConfigTable[cfg].kernel, a);
@@ -60,12 +62,17 @@ cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
     const int kernel = kConfigTable[cfg].kernel;
     if (kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
+    if (kernel == kKernTf32x3_128x256) return launch_tf32x3(g, stream);
     if (kernel >= kKernLadderNaive) return launch_ladder(kernel, g, stream);
     GemmArgs a = g;
     if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
     return launch_ffma_tma(kConfigTable[cfg].kernel, a, stream);
 }
 
-cudaError_t configs_prepare_device() { return prepare_ffma_tma(); }
+cudaError_t configs_prepare_device()
+{
+    const cudaError_t e = prepare_ffma_tma();
+    return e != cudaSuccess ? e : prepare_tf32x3();
+}
 
 }  // namespace sgemm_gb300

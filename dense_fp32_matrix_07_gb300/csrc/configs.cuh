@@ -28,7 +28,9 @@ enum KernelId : int {
     kKernLadderNaive,           // one thread per output, threadIdx.x -> row
     kKernLadderCoalesced,       // one thread per output, threadIdx.x -> column
     kKernLadderCacheBlocked8x8, // 8x8 register micro-tiles, caches only
-    kKernLadderRegisterTiled2x2 // 16x16 padded smem tiles, 2x2 per thread
+    kKernLadderRegisterTiled2x2, // 16x16 padded smem tiles, 2x2 per thread
+    // Tensor cores (kernels_tf32x3.cu): 3xTF32 split, tcgen05.mma into TMEM.
+    kKernTf32x3_128x256
 };
 
 // Configurations = kernel instance + schedule policy.
@@ -47,6 +49,7 @@ enum ConfigId : int {
     kCfgLadderCoalesced,
     kCfgLadderCacheBlocked8x8,
     kCfgLadderRegisterTiled2x2,
+    kCfgTf32x3_128x256,
     kNumConfigs
 };
 
@@ -54,7 +57,8 @@ struct ConfigInfo {
     const char *name;
     int kernel;      // KernelId
     int sched;       // SchedPolicy
-    bool uses_tma;   // reads A and B through TMA tensor maps
+    bool uses_tma;   // TMA tensor maps (32-bit coordinates)
+    bool packs;      // needs A and B with 16-byte-aligned rows (packs others)
     int bm, bn;      // block tile
 };
 
@@ -84,5 +88,11 @@ cudaError_t prepare_ffma_tma();
 
 // Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
 cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);
+
+// The 3xTF32 tensor-core path (kernels_tf32x3.cu): split pre-passes into
+// g.workspace, then the tcgen05 product.
+cudaError_t launch_tf32x3(const GemmArgs &g, cudaStream_t stream);
+size_t tf32x3_workspace_bytes(const GemmArgs &g);
+cudaError_t prepare_tf32x3();
 
 }  // namespace sgemm_gb300

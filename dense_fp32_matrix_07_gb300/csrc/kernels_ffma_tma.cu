@@ -54,30 +54,6 @@ namespace sgemm_gb300 {
 
 namespace {
 
-// Wall-clock limit of one bounded wait, in nanoseconds.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
-
-__device__ __forceinline__ uint64_t global_timer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for phase `parity` of the mbarrier at `bar`; false after kWaitLimitNs.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
-{
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 0; n < kSpinLimit; ++n) {
-#pragma unroll 1
-        for (int r = 0; r < 16; ++r)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return false;
-}
-
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
 {
     unsigned v;
@@ -94,11 +70,11 @@ __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
 __device__ __forceinline__ bool wait_flag(const unsigned *flag)
 {
     if (ld_acquire_gpu(flag) != 0) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint64_t t0 = ptx::global_timer_ns();
     for (uint32_t n = 0; n < kSpinLimit; ++n) {
         __nanosleep(64);
         if (ld_acquire_gpu(flag) != 0) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (ptx::global_timer_ns() - t0 > ptx::kWaitLimitNs) return false;
     }
     return false;
 }
@@ -279,7 +255,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
                 const int s = (int)(it % STAGES);
                 const int round = (int)(it / STAGES);
-                if (!wait_phase(empty_bar(s), (round & 1) ^ 1)) {
+                if (!ptx::wait_phase(empty_bar(s), (round & 1) ^ 1)) {
                     atomicOr(status, kStatusTimeout);
                     ok = false;
                     break;
@@ -295,7 +271,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         // Every issued copy must land before this CTA's shared memory goes away.
         for (int s = 0; s < STAGES; ++s) {
-            if (last_round[s] >= 0 && !wait_phase(full_bar(s), last_round[s] & 1)) {
+            if (last_round[s] >= 0 && !ptx::wait_phase(full_bar(s), last_round[s] & 1)) {
                 atomicOr(status, kStatusTimeout);
             }
         }
@@ -334,8 +310,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
 
         for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
             const int s = (int)(it % STAGES);
-            if (!wait_phase(full_bar(s), (it / STAGES) & 1)) {
-                atomicOr(status, kStatusTimeout);
+            if (!ptx::wait_phase_warp(full_bar(s), (it / STAGES) & 1)) {
+                if (lane == 0) atomicOr(status, kStatusTimeout);
                 return;
             }
             const uint8_t *As = base_ptr + s * Cfg::A_BYTES + a_row_off;
@@ -410,8 +386,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             // This CTA owns the tile: add the later CTAs' partial sums in order.
             const int64_t tile_end = (item.tile - sched.dp_tiles + 1) * sched.nk;
             for (int h = g + 1; h < sched.sk_ctas && sk_start(sched, h) < tile_end; ++h) {
-                if (!wait_flag(sched.flags + (int64_t)h * Cfg::CONSUMERS + warp)) {
-                    atomicOr(status, kStatusTimeout);
+                if (!__all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)h * Cfg::CONSUMERS + warp))) {
+                    if (lane == 0) atomicOr(status, kStatusTimeout);
                     return;
                 }
                 const float4 *slot = reinterpret_cast<const float4 *>(sched.partials + (int64_t)h * BM * BN);

@@ -1,0 +1,395 @@
+// FP32 product on the 5th-generation tensor cores by 3xTF32 splitting.
+//
+// Chapter 9: Optimised Matrix Multiplication, section 9.7, points past CUDA
+// cores to tensor-core instructions that multiply whole tiles on a separate
+// pipeline. Those take TF32 inputs (10 explicit mantissa bits), so each FP32
+// operand is split as x = hi + lo with hi = tf32(x) and lo = tf32(x - hi),
+// and the product keeps three of the four terms:
+//     A.B ~ A_hi.B_hi + A_hi.B_lo + A_lo.B_hi      (A_lo.B_lo, ~2^-22 |A||B|, dropped)
+// accumulated in FP32 in tensor memory. Integer-valued inputs with
+// |x| < 2^11 have lo = 0 and stay exact; non-finite inputs do not (x - hi is
+// NaN for infinite x), so this path is documented for finite inputs.
+//
+// Data flow of one call: two split pre-passes write A_hi, A_lo (M x Kp,
+// K-major) and B_hi^T, B_lo^T (N x Kp, K-major: B is transposed on the way)
+// into scratch; the product kernel then streams 128 x 16 and 256 x 16 tiles
+// of all four through TMA (64-byte swizzle) into a 4-stage ring.
+//
+// Product kernel: persistent, one 128 x 256 output tile at a time per CTA.
+//   warp 0      TMA producer (one thread): 4 boxes per K slab, full/empty
+//               mbarriers per stage;
+//   warp 1      MMA issuer (one thread) and TMEM owner: per K slab of 16,
+//               2 x 3 tcgen05.mma .kind::tf32 (M 128, N 256, K 8) into a
+//               TMEM accumulator; tcgen05.commit frees the stage, and at the
+//               end of a tile signals the epilogue;
+//   warps 4-7   epilogue: warp 4+q reads TMEM lanes 32q..32q+31 (rows of the
+//               tile) with tcgen05.ld and stores them to C.
+// The accumulator is double-buffered (2 x 256 of the 512 TMEM columns), so
+// the epilogue of one tile overlaps the MMAs of the next. Every wait is
+// bounded in time; a role that gives up sets the device error word and skips
+// to the teardown (a named barrier of the MMA and epilogue warps, then TMEM
+// is freed); the producer drains its own copies before leaving.
+#include "common.cuh"
+#include "configs.cuh"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace sgemm_gb300 {
+
+namespace {
+
+struct Tf32x3Cfg {
+    static constexpr int BM = 128, BN = 256, BK = 16, STAGES = 4;
+    static constexpr int ROW_BYTES = BK * 4;                   // 64: 64-byte swizzle
+    static constexpr int A_TILE = BM * ROW_BYTES;              // 8 KB
+    static constexpr int B_TILE = BN * ROW_BYTES;              // 16 KB
+    static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;    // full, empty, acc full, acc empty, drain
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int TMEM_COLS = 2 * BN;                   // double-buffered FP32 accumulator
+    static constexpr int THREADS = 256;
+    static constexpr int EPI_WARP0 = 4;
+    static constexpr uint32_t IDESC = ptx::idesc_tf32_kmajor(BM, BN);
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(TMEM_COLS <= 512, "tensor memory columns");
+};
+
+__device__ __forceinline__ void tile_coords_g8(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
+{
+    constexpr int GR = 8;
+    const int64_t per_group = (int64_t)GR * tiles_n;
+    const int64_t group = t / per_group;
+    const int first_m = (int)(group * GR);
+    const int rows = min(tiles_m - first_m, GR);
+    const int64_t local = t - group * per_group;
+    tm = first_m + (int)(local % rows);
+    tn = (int)(local / rows);
+}
+
+template <bool VEC_C>
+__global__ void __launch_bounds__(Tf32x3Cfg::THREADS, 1)
+sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_constant__ CUtensorMap mapAlo,
+                    const __grid_constant__ CUtensorMap mapBhi, const __grid_constant__ CUtensorMap mapBlo,
+                    float *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned int *status)
+{
+    using Cfg = Tf32x3Cfg;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bars = base + STAGES * Cfg::STAGE_BYTES;
+    auto stage_a_hi = [&](int s) { return base + s * Cfg::STAGE_BYTES; };
+    auto stage_a_lo = [&](int s) { return base + s * Cfg::STAGE_BYTES + Cfg::A_TILE; };
+    auto stage_b_hi = [&](int s) { return base + s * Cfg::STAGE_BYTES + 2 * Cfg::A_TILE; };
+    auto stage_b_lo = [&](int s) { return base + s * Cfg::STAGE_BYTES + 2 * Cfg::A_TILE + Cfg::B_TILE; };
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    const uint32_t tmem_slot = bars + 8u * Cfg::NUM_BARS;
+    uint32_t *tmem_slot_ptr = reinterpret_cast<uint32_t *>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int64_t tiles = (int64_t)tiles_m * tiles_n;
+    const int nk = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf_bar(b), 1);
+            ptx::mbar_init(acce_bar(b), 4);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init_fence();
+    }
+    if (warp == 1) ptx::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t taddr = *tmem_slot_ptr;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane != 0) return;
+        ptx::prefetch_tensormap(&mapAhi);
+        ptx::prefetch_tensormap(&mapAlo);
+        ptx::prefetch_tensormap(&mapBhi);
+        ptx::prefetch_tensormap(&mapBlo);
+        const uint64_t policy = ptx::policy_evict_last();
+        int last_round[STAGES];
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords_g8(t, tiles_m, tiles_n, tm, tn);
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int s = (int)(it % STAGES);
+                const int round = (int)(it / STAGES);
+                if (!ptx::wait_phase(empty_bar(s), (round & 1) ^ 1)) {
+                    atomicOr(status, kStatusTimeout);
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+                ptx::tma_load_2d(stage_a_hi(s), &mapAhi, full_bar(s), kb * BK, tm * BM, policy);
+                ptx::tma_load_2d(stage_a_lo(s), &mapAlo, full_bar(s), kb * BK, tm * BM, policy);
+                ptx::tma_load_2d(stage_b_hi(s), &mapBhi, full_bar(s), kb * BK, tn * BN, policy);
+                ptx::tma_load_2d(stage_b_lo(s), &mapBlo, full_bar(s), kb * BK, tn * BN, policy);
+                last_round[s] = round;
+            }
+        }
+        for (int s = 0; s < STAGES; ++s)
+            if (last_round[s] >= 0 && !ptx::wait_phase(full_bar(s), last_round[s] & 1))
+                atomicOr(status, kStatusTimeout);
+        return;
+    }
+    if (warp == 2 || warp == 3) return;
+
+    if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            uint32_t it = 0, lt = 0;
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+                const int b = (int)(lt & 1);
+                const uint32_t use = lt >> 1;
+                if (!ptx::wait_phase(acce_bar(b), (use & 1) ^ 1)) {
+                    atomicOr(status, kStatusTimeout);
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = taddr + (uint32_t)(b * BN);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = (int)(it % STAGES);
+                    if (!ptx::wait_phase(full_bar(s), (it / STAGES) & 1)) {
+                        atomicOr(status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < BK / 8; ++ks) {
+                        const uint64_t ah = ptx::sdesc_kmajor(stage_a_hi(s) + ks * 32, Cfg::ROW_BYTES);
+                        const uint64_t al = ptx::sdesc_kmajor(stage_a_lo(s) + ks * 32, Cfg::ROW_BYTES);
+                        const uint64_t bh = ptx::sdesc_kmajor(stage_b_hi(s) + ks * 32, Cfg::ROW_BYTES);
+                        const uint64_t bl = ptx::sdesc_kmajor(stage_b_lo(s) + ks * 32, Cfg::ROW_BYTES);
+                        ptx::mma_tf32(d, ah, bh, Cfg::IDESC, (kb | ks) ? 1u : 0u);
+                        ptx::mma_tf32(d, ah, bl, Cfg::IDESC, 1u);
+                        ptx::mma_tf32(d, al, bh, Cfg::IDESC, 1u);
+                    }
+                    ptx::mma_commit(empty_bar(s));   // the stage is free once these MMAs are done
+                }
+                if (!ok) break;
+                ptx::mma_commit(accf_bar(b));        // the tile's accumulator is complete
+            }
+            // Every MMA issued above must finish before TMEM is released.
+            ptx::mma_commit(drain_bar);
+            if (!ptx::wait_phase(drain_bar, 0)) atomicOr(status, kStatusTimeout);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int q = warp - Cfg::EPI_WARP0;          // TMEM lane quarter (== warp % 4)
+        uint32_t lt = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+            const int b = (int)(lt & 1);
+            const uint32_t use = lt >> 1;
+            if (!ptx::wait_phase_warp(accf_bar(b), use & 1)) {
+                if (lane == 0) atomicOr(status, kStatusTimeout);
+                break;
+            }
+            ptx::tc_fence_after();
+            int tm, tn;
+            tile_coords_g8(t, tiles_m, tiles_n, tm, tn);
+            const int64_t row = (int64_t)tm * BM + 32 * q + lane;
+            float *crow = C + row * ldc;
+            const int col_base = tn * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                ptx::tmem_ld32(taddr + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + c0), v);
+                ptx::tmem_ld_wait();
+                if (c0 == BN - 32) {
+                    // Last read of this accumulator: hand it back to the MMA warp.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce_bar(b));
+                }
+                if (row < M) {
+                    const int col0 = col_base + c0;
+                    if (VEC_C && col0 + 32 <= N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(crow + col0 + j) =
+                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+        ptx::tc_fence_before();
+    }
+
+    // ------------------------------ teardown ------------------------------
+    ptx::named_barrier(1, 32 * 5);                    // MMA warp + 4 epilogue warps
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(taddr, Cfg::TMEM_COLS);
+    }
+}
+
+// hi[i * ldo + k] = tf32(x), lo[i * ldo + k] = tf32(x - hi) for x = src[i * ld + k].
+__global__ void tf32_split_rows_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t ld,
+                                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldo)
+{
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x) {
+            const float x = src[r * ld + c];
+            const float h = ptx::to_tf32(x);
+            hi[r * ldo + c] = h;
+            lo[r * ldo + c] = ptx::to_tf32(x - h);
+        }
+    }
+}
+
+// The same split of B (K x N, leading dimension ld), written transposed:
+// hiT[n * ldo + k], loT[n * ldo + k]. 32 x 32 tiles through shared memory so
+// both the reads (along n) and the writes (along k) are coalesced.
+__global__ void tf32_split_transpose_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
+                                            int64_t ld, float *__restrict__ hiT, float *__restrict__ loT,
+                                            int64_t ldo)
+{
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8 threads
+    const int64_t tiles_c = (cols + 31) / 32;
+    const int64_t ntiles = ((rows + 31) / 32) * tiles_c;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int64_t r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
+            tile[ty + 8 * i][tx] = (r < rows && c < cols) ? src[r * ld + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;   // output row c, column r
+            if (c < cols && r < rows) {
+                const float x = tile[tx][ty + 8 * i];
+                const float h = ptx::to_tf32(x);
+                hiT[c * ldo + r] = h;
+                loT[c * ldo + r] = ptx::to_tf32(x - h);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+int64_t round_up_i(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct Tf32x3Layout {
+    int64_t kp;                  // leading dimension of the split operands
+    size_t a_bytes, b_bytes;     // one split copy of A / of B^T, 256-byte rounded
+    size_t total;
+};
+
+Tf32x3Layout tf32x3_layout(const GemmArgs &g)
+{
+    Tf32x3Layout l;
+    l.kp = round_up_i(g.K, 4);
+    l.a_bytes = (size_t)round_up_i(g.M * l.kp * 4, 256);
+    l.b_bytes = (size_t)round_up_i(g.N * l.kp * 4, 256);
+    l.total = 2 * l.a_bytes + 2 * l.b_bytes;
+    return l;
+}
+
+cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int64_t k, int64_t ld, int box_rows)
+{
+    void *fnp = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fnp, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fnp) return cudaErrorNotSupported;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fnp);
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)Tf32x3Cfg::BK, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
+                              box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t tf32x3_workspace_bytes(const GemmArgs &g) { return tf32x3_layout(g).total; }
+
+cudaError_t prepare_tf32x3()
+{
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tf32x3_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tf32x3Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tf32x3_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Tf32x3Cfg::SMEM_BYTES);
+}
+
+cudaError_t launch_tf32x3(const GemmArgs &g, cudaStream_t stream)
+{
+    const Tf32x3Layout l = tf32x3_layout(g);
+    if (!g.workspace || g.workspace_bytes < l.total) return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(g.workspace);
+    float *a_hi = reinterpret_cast<float *>(ws);
+    float *a_lo = reinterpret_cast<float *>(ws + l.a_bytes);
+    float *b_hi = reinterpret_cast<float *>(ws + 2 * l.a_bytes);
+    float *b_lo = reinterpret_cast<float *>(ws + 2 * l.a_bytes + l.b_bytes);
+
+    // Split pre-passes.
+    {
+        const int64_t gy = g.M < 65535 ? g.M : 65535;
+        int64_t gx = (g.K + 255) / 256;
+        if (gx > 64) gx = 64;
+        tf32_split_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(g.A, g.M, g.K, g.lda, a_hi,
+                                                                                   a_lo, l.kp);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int64_t tiles = ((g.K + 31) / 32) * ((g.N + 31) / 32);
+        const unsigned grid = (unsigned)(tiles < (int64_t)g.num_sms * 32 ? tiles : (int64_t)g.num_sms * 32);
+        tf32_split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(g.B, g.K, g.N, g.ldb, b_hi, b_lo, l.kp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    CUtensorMap mAh, mAl, mBh, mBl;
+    cudaError_t e;
+    if ((e = encode_kmajor(&mAh, a_hi, g.M, g.K, l.kp, Tf32x3Cfg::BM)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mAl, a_lo, g.M, g.K, l.kp, Tf32x3Cfg::BM)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Tf32x3Cfg::BN)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Tf32x3Cfg::BN)) != cudaSuccess) return e;
+    const int64_t tiles = ((g.M + Tf32x3Cfg::BM - 1) / Tf32x3Cfg::BM) * ((g.N + Tf32x3Cfg::BN - 1) / Tf32x3Cfg::BN);
+    const unsigned grid = (unsigned)(tiles < g.num_sms ? tiles : g.num_sms);
+    const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
+    if (vec)
+        sgemm_tf32x3_kernel<true><<<grid, Tf32x3Cfg::THREADS, Tf32x3Cfg::SMEM_BYTES, stream>>>(
+            mAh, mAl, mBh, mBl, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+    else
+        sgemm_tf32x3_kernel<false><<<grid, Tf32x3Cfg::THREADS, Tf32x3Cfg::SMEM_BYTES, stream>>>(
+            mAh, mAl, mBh, mBl, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm_gb300

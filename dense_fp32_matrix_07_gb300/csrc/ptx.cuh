@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "common.cuh"
+
 namespace sgemm_gb300 {
 namespace ptx {
 
@@ -52,6 +54,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// Wall-clock limit of one bounded wait, in nanoseconds.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for phase `parity` of the mbarrier at `bar`; false after about
+// kWaitLimitNs of wall clock (kSpinLimit probe rounds as a backstop).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0; n < kSpinLimit; ++n) {
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// wait_phase() with one answer for the whole (converged) warp: a lane whose
+// own clock ran out while another saw the phase complete must not leave the
+// warp half-way through warp-collective code.
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity)
+{
+    return __all_sync(0xffffffffu, wait_phase(bar, parity)) != 0;
+}
+
 // Register reallocation between the warpgroups of a CTA (all 128 threads of
 // a warpgroup execute the same instruction).
 template <int REGS>
@@ -91,6 +126,98 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory).
+// ----------------------------------------------------------------------------
+
+// Instruction descriptor of tcgen05.mma .kind::tf32 with FP32 accumulation,
+// both operands K-major: D format F32 (bits 4-5 = 1), A and B format TF32
+// (bits 7-9 and 10-12 = 2), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_tf32_kmajor(int m, int n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored as rows of
+// `row_bytes` (64 or 128) with the matching TMA swizzle: start address >> 4
+// (bits 0-13), stride between 8-row groups >> 4 (bits 32-45), descriptor
+// version 1 (bit 46), swizzle mode at bits 61-63 (2: 128-byte, 4: 64-byte).
+// The leading offset is unused for swizzled K-major operands.
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t smem_addr, int row_bytes)
+{
+    const uint64_t swizzle = row_bytes == 128 ? 2 : 4;
+    return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)((8 * row_bytes) >> 4) << 32) | ((uint64_t)1 << 46) | (swizzle << 61);
+}
+
+// TMEM allocation (one whole warp); the address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one thread issues.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier receives one arrival once every earlier tcgen05 operation of
+// this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes: thread i gets lane i.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                   "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                   "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+                   "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+                   "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// FP32 -> TF32, round to nearest (ties away); the low 13 bits come out zero.
+__device__ __forceinline__ float to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 
 }  // namespace ptx

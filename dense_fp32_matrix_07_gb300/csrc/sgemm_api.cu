@@ -165,10 +165,10 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_
     if (num_sms <= 0) return SGEMM_ERR_INVALID_VALUE;
     const ProblemShape p{M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms};
     const int cfg = select_config(p);
-    const bool tma = kConfigTable[cfg].uses_tma;
+    const bool packs = kConfigTable[cfg].packs;
     if (out_config) *out_config = cfg;
-    if (out_pack_a) *out_pack_a = (tma && needs_pack(a_addr, lda)) ? 1 : 0;
-    if (out_pack_b) *out_pack_b = (tma && needs_pack(b_addr, ldb)) ? 1 : 0;
+    if (out_pack_a) *out_pack_a = (packs && needs_pack(a_addr, lda)) ? 1 : 0;
+    if (out_pack_b) *out_pack_b = (packs && needs_pack(b_addr, ldb)) ? 1 : 0;
     return SGEMM_OK;
 }
 
@@ -214,8 +214,8 @@ static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
     g.withhold_it = withhold_it;
     // One scratch allocation, carved into: packed A, packed B (rows padded to
     // a multiple of 32 floats = 128 bytes), then the stream-K workspace.
-    const bool tma = kConfigTable[cfg].uses_tma;
-    const bool pa = tma && needs_pack(a, lda), pb = tma && needs_pack(b, ldb);
+    const bool packs = kConfigTable[cfg].packs;
+    const bool pa = packs && needs_pack(a, lda), pb = packs && needs_pack(b, ldb);
     const int64_t lda_p = round_up(K, 32), ldb_p = round_up(N, 32);
     const size_t a_bytes = pa ? (size_t)(M * lda_p) * 4 : 0;
     const size_t b_bytes = pb ? (size_t)(K * ldb_p) * 4 : 0;

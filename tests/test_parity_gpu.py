@@ -151,10 +151,10 @@ def test_invalid_arguments_launch_nothing(cuda_device):
 # the launch the bench times).
 # --------------------------------------------------------------------------
 
-def _run_workload(w, dist=None):
+def _run_workload(w, dist=None, config=-1):
     dist = dist or w.dist
     A, B = workloads.make_operands(w.M, w.N, w.K, dist, w.seed, w.lda, w.ldb)
-    rc, C, dC = run(w.M, w.N, w.K, A, w.lda, B, w.ldb, ldc=w.ldc, c_fill=float("nan"))
+    rc, C, dC = run(w.M, w.N, w.K, A, w.lda, B, w.ldb, ldc=w.ldc, c_fill=float("nan"), config=config)
     assert rc == 0
     check_untouched_padding(dC, w.N)
     return A, B, C
@@ -187,6 +187,20 @@ def test_workload_sampled_check(cuda_device, oracle, name, dist):
     print(f"{name} {dist or w.dist}: max |diff|/S = {r:.3e}")
     del A, B, C
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["rect4097x3001x2049", "sq4096", "sq16384"])
+def test_tf32x3_tensor_core_path_at_full_size(cuda_device, oracle, name):
+    """The 3xTF32 tcgen05 path at the full workload sizes: sampled rows and
+    columns within 1e-4 * sum|A_ik B_kj| (float) and bit-exact (integers)."""
+    w = workloads.WORKLOADS[name]
+    cfg = sg.config_ids()["tf32x3_128x256_k16_s4"]
+    for dist in (None, "int"):
+        A, B, C = _run_workload(w, dist, config=cfg)
+        r = _sampled_check(oracle, w, A, B, C, dist == "int")
+        print(f"tf32x3 {name} {dist or w.dist}: max |diff|/S = {r:.3e}")
+        del A, B, C
+        torch.cuda.empty_cache()
 
 
 def test_status_is_clean_after_the_suite(cuda_device):
