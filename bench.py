@@ -113,6 +113,19 @@ def profiled_traffic(config_name: str):
     return float(val.group(1))
 
 
+def measured_tf32_tflops() -> tuple:
+    """(TF32 dense tensor peak in TFLOP/s, basis): the measured BF16 burst
+    peak scaled by the nominal TF32/BF16 ratio 1.1/2.25, else the profiling
+    recipe's fallback BF16 figure (1.9 PFLOP/s) scaled the same way."""
+    ratio = 1.1 / 2.25
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        return bf16 * ratio, f"measured BF16 {bf16:.1f} TF x 1.1/2.25 (nominal TF32/BF16)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0 * ratio, "fallback BF16 1900 TF x 1.1/2.25 (nominal TF32/BF16)"
+
+
 def measured_sm_max_mhz() -> float:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -315,6 +328,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs (config sweeps)")
+    ap.add_argument("--no-tf32x3", action="store_true",
+                    help="skip the separately reported 3xTF32 tensor-core measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -481,6 +496,44 @@ def main():
         e2e_value = job_gflops(flops, e2e_steps, world, e2e_s)
         serial_value = job_gflops(flops, e2e_steps, world, serial_s)
 
+    # ---- the optional 3xTF32 tensor-core path, reported separately ----
+    tc = None
+    if not args.no_tf32x3 and args.config < 0:
+        tc_cfg = sg.config_ids()["tf32x3_128x256_k16_s4"]
+
+        def tc_step():
+            r = sg.sgemm_ex(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
+                            dC.data_ptr(), w.ldc, tc_cfg, sh)
+            if r != 0:
+                raise RuntimeError(sg.sgemm_error_string(r))
+
+        for _ in range(3):
+            tc_step()
+        torch.cuda.synchronize()
+        tc_steps = max(3, min(args.steps, 50))
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(tc_steps):
+            if flush is not None:
+                flush.zero_()
+            tc_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if sg.sgemm_check_status(sh) != 0:
+            raise RuntimeError("device status after the 3xTF32 steps")
+        (tc_s,) = max_over_ranks([ev0.elapsed_time(ev1) / 1e3], pg, dev)
+        tc_value = job_gflops(flops, tc_steps, world, tc_s)
+        tf32_peak, tf32_basis = measured_tf32_tflops()
+        tensor_tflops = 3 * flops * tc_steps / tc_s / 1e12   # three TF32 products per FP32 product
+        tc = {"value": round(tc_value, 1), "unit": "GFLOP/s", "config": "tf32x3_128x256_k16_s4",
+              "steps": tc_steps, "launches_per_step": 3,
+              "note": "FP32 result from three TF32 tensor-core products (hi.hi + hi.lo + lo.hi), "
+                      "same 1e-4 * sum|A_ik B_kj| tolerance; includes the split pre-passes",
+              "roofline": {"bound": "tensor", "achieved": round(tensor_tflops, 1),
+                           "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                           "frac": round(tensor_tflops / tf32_peak, 4), "peak_basis": tf32_basis}}
+
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -521,6 +574,7 @@ def main():
                                    f"{sm_max:.0f} MHz (max SM clock)"},
         "clocks": clocks,
         "host_elapsed_s": round(elapsed_host, 3),
+        "tensor_core_3xtf32": tc,
     }
     if clocks and clocks.get("sm_mhz"):
         line["roofline"]["frac_at_sampled_clock"] = round(

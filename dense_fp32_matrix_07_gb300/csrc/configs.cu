@@ -19,6 +19,9 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, false, 128, 128},
     {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, false, 16, 16},
     {"tf32x3_128x256_k16_s4", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
+    {"tf32x3_128x256_k16_s4_sk", kKernTf32x3_128x256, kSchedStreamK, true, false, 128, 256},
+    {"tf32x3_128x256_k16_s4_auto", kKernTf32x3_128x256, kSchedAuto, true, false, 128, 256},
+    {"tf32x3_128x128_k16_s6", kKernTf32x3_128x128, kSchedDataParallel, true, false, 128, 128},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
@@ -52,7 +55,11 @@ int select_config(const ProblemShape &p)
 size_t config_workspace_bytes(int cfg, const GemmArgs &g)
 {
     if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].uses_tma) return 0;
-    if (kConfigTable[cfg].kernel == kKernTf32x3_128x256) return tf32x3_workspace_bytes(g);
+    if (kConfigTable[cfg].kernel >= kKernTf32x3_128x256) {
+        GemmArgs a = g;
+        a.sched = kConfigTable[cfg].sched;
+        return tf32x3_workspace_bytes(kConfigTable[cfg].kernel, a);
+    }
     GemmArgs a = g;
     a.sched = kConfigTable[cfg].sched;
     return ffma_tma_workspace_bytes(kConfigTable[cfg].kernel, a);
@@ -62,7 +69,11 @@ cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
     const int kernel = kConfigTable[cfg].kernel;
     if (kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
-    if (kernel == kKernTf32x3_128x256) return launch_tf32x3(g, stream);
+    if (kernel >= kKernTf32x3_128x256) {
+        GemmArgs a = g;
+        if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
+        return launch_tf32x3(kernel, a, stream);
+    }
     if (kernel >= kKernLadderNaive) return launch_ladder(kernel, g, stream);
     GemmArgs a = g;
     if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;

@@ -30,7 +30,8 @@ enum KernelId : int {
     kKernLadderCacheBlocked8x8, // 8x8 register micro-tiles, caches only
     kKernLadderRegisterTiled2x2, // 16x16 padded smem tiles, 2x2 per thread
     // Tensor cores (kernels_tf32x3.cu): 3xTF32 split, tcgen05.mma into TMEM.
-    kKernTf32x3_128x256
+    kKernTf32x3_128x256,
+    kKernTf32x3_128x128
 };
 
 // Configurations = kernel instance + schedule policy.
@@ -50,6 +51,9 @@ enum ConfigId : int {
     kCfgLadderCacheBlocked8x8,
     kCfgLadderRegisterTiled2x2,
     kCfgTf32x3_128x256,
+    kCfgTf32x3_128x256_sk,
+    kCfgTf32x3_128x256_auto,
+    kCfgTf32x3_128x128,
     kNumConfigs
 };
 
@@ -91,8 +95,8 @@ cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);
 
 // The 3xTF32 tensor-core path (kernels_tf32x3.cu): split pre-passes into
 // g.workspace, then the tcgen05 product.
-cudaError_t launch_tf32x3(const GemmArgs &g, cudaStream_t stream);
-size_t tf32x3_workspace_bytes(const GemmArgs &g);
+cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream);
+size_t tf32x3_workspace_bytes(int kernel, const GemmArgs &g);
 cudaError_t prepare_tf32x3();
 
 }  // namespace sgemm_gb300

@@ -45,6 +45,7 @@
 #include "common.cuh"
 #include "configs.cuh"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,31 +54,6 @@
 namespace sgemm_gb300 {
 
 namespace {
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Waits until *flag != 0; false after kWaitLimitNs.
-__device__ __forceinline__ bool wait_flag(const unsigned *flag)
-{
-    if (ld_acquire_gpu(flag) != 0) return true;
-    const uint64_t t0 = ptx::global_timer_ns();
-    for (uint32_t n = 0; n < kSpinLimit; ++n) {
-        __nanosleep(64);
-        if (ld_acquire_gpu(flag) != 0) return true;
-        if (ptx::global_timer_ns() - t0 > ptx::kWaitLimitNs) return false;
-    }
-    return false;
-}
 
 template <int BM_, int BN_, int BK_, int STAGES_, int TN_, bool PAIRED_, int MIN_BLOCKS_>
 struct FfmaTmaCfg {
@@ -125,84 +101,6 @@ struct FfmaTmaCfg {
                                     LAUNCH_REGS * THREADS,
                   "register split exceeds the launch allocation");
 };
-
-// The work schedule, computed on the host (make_schedule) and read by every
-// thread. See the file comment.
-struct Schedule {
-    int tiles_m, tiles_n;
-    int nk;             // K slabs per tile
-    int grid;           // CTAs launched
-    int64_t tiles;      // all output tiles
-    int64_t dp_tiles;   // whole-tile work: tiles [0, dp_tiles), round-robin
-    int64_t sk_iters;   // slab iterations of the stream-K region
-    int sk_ctas;        // CTAs [0, sk_ctas) share those iterations
-    unsigned *flags;    // sk_ctas x CONSUMERS flags (zeroed before launch)
-    float *partials;    // sk_ctas slots of BM x BN floats
-};
-
-// One unit of work: slabs [kb0, kb1) of output tile `tile`.
-struct Item {
-    int64_t tile;
-    int kb0, kb1;
-};
-
-struct Cursor {
-    int64_t dp_next;        // next whole tile of this CTA
-    int64_t sk_pos, sk_end; // this CTA's stream-K iteration range
-};
-
-__device__ __forceinline__ int64_t sk_start(const Schedule &s, int g)
-{
-    return s.sk_iters * g / s.sk_ctas;
-}
-
-__device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
-{
-    Cursor c;
-    c.dp_next = g;
-    if (g < s.sk_ctas) {
-        c.sk_pos = sk_start(s, g);
-        c.sk_end = sk_start(s, g + 1);
-    } else {
-        c.sk_pos = c.sk_end = 0;
-    }
-    return c;
-}
-
-__device__ __forceinline__ bool next_item(const Schedule &s, Cursor &c, Item &it)
-{
-    if (c.dp_next < s.dp_tiles) {
-        it.tile = c.dp_next;
-        it.kb0 = 0;
-        it.kb1 = s.nk;
-        c.dp_next += s.grid;
-        return true;
-    }
-    if (c.sk_pos < c.sk_end) {
-        const int64_t rel = c.sk_pos / s.nk;
-        it.tile = s.dp_tiles + rel;
-        it.kb0 = (int)(c.sk_pos - rel * s.nk);
-        const int64_t left = c.sk_end - c.sk_pos;
-        it.kb1 = (int)(left < s.nk - it.kb0 ? it.kb0 + left : s.nk);
-        c.sk_pos += it.kb1 - it.kb0;
-        return true;
-    }
-    return false;
-}
-
-// Output tile of linear index t: groups of 8 block rows, column-major inside
-// a group, so the CTAs running at the same time touch few A and B panels.
-__device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
-{
-    constexpr int GR = 8;
-    const int64_t per_group = (int64_t)GR * tiles_n;
-    const int64_t group = t / per_group;
-    const int first_m = (int)(group * GR);
-    const int rows = min(tiles_m - first_m, GR);
-    const int64_t local = t - group * per_group;
-    tm = first_m + (int)(local % rows);
-    tn = (int)(local / rows);
-}
 
 template <class Cfg, bool VEC_C>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
@@ -482,56 +380,18 @@ cudaError_t set_smem_limit()
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
 }
 
-constexpr size_t kFlagBytesAlign = 256;
-
-size_t round_up_bytes(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// The schedule of a product (without workspace pointers). `with_sk` false
-// gives the whole-tile schedule.
+// The schedule of a product; `with_sk` false gives whole tiles only.
 template <class Cfg>
 Schedule make_schedule(const GemmArgs &g, bool with_sk)
 {
-    Schedule s{};
-    s.tiles_m = (int)((g.M + Cfg::BM - 1) / Cfg::BM);
-    s.tiles_n = (int)((g.N + Cfg::BN - 1) / Cfg::BN);
-    s.nk = (int)((g.K + Cfg::BK - 1) / Cfg::BK);
-    s.tiles = (int64_t)s.tiles_m * s.tiles_n;
-    const int64_t slots = (int64_t)g.num_sms * Cfg::MIN_BLOCKS;
-    s.dp_tiles = s.tiles;
-    s.sk_iters = 0;
-    s.sk_ctas = 0;
-    s.grid = (int)(s.tiles < slots ? s.tiles : slots);
-    bool sk = false;
-    if (with_sk && g.sched == kSchedStreamK) {
-        sk = true;
-    } else if (with_sk && g.sched == kSchedAuto) {
-        // Stream-K only when whole tiles would leave the last wave short:
-        // efficiency = tiles / (rounds * slots) below 97%.
-        const int64_t rounds = (s.tiles + slots - 1) / slots;
-        sk = (double)s.tiles < 0.97 * (double)(rounds * slots) && s.nk >= 8;
-    }
-    if (!sk) return s;
-    const int64_t full_rounds = s.tiles / slots;
-    const int64_t dp_rounds = (g.sched == kSchedStreamK || full_rounds < 1) ? 0 : full_rounds - 1;
-    s.dp_tiles = dp_rounds * slots;
-    s.sk_iters = (s.tiles - s.dp_tiles) * s.nk;
-    // Forced stream-K splits as finely as one slab per CTA (to exercise the
-    // fix-up path); the automatic choice keeps at least 4 slabs per CTA.
-    const int64_t min_iters = g.sched == kSchedStreamK ? 1 : 4;
-    int64_t ctas = s.sk_iters / min_iters;
-    if (ctas > slots) ctas = slots;
-    if (ctas < 1) ctas = 1;
-    s.sk_ctas = (int)ctas;
-    s.grid = (int)(s.dp_tiles > 0 ? slots : ctas);
-    return s;
+    return plan_schedule(g.M, g.N, g.K, Cfg::BM, Cfg::BN, Cfg::BK, g.num_sms * Cfg::MIN_BLOCKS, g.sched,
+                         with_sk);
 }
 
 template <class Cfg>
 size_t workspace_bytes(const Schedule &s)
 {
-    if (s.sk_ctas == 0) return 0;
-    return round_up_bytes((size_t)s.sk_ctas * Cfg::CONSUMERS * sizeof(unsigned), kFlagBytesAlign) +
-           (size_t)s.sk_ctas * Cfg::BM * Cfg::BN * sizeof(float);
+    return schedule_workspace_bytes(s, Cfg::CONSUMERS, Cfg::BM, Cfg::BN);
 }
 
 template <class Cfg>
@@ -545,14 +405,8 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     // Stream-K needs the caller's workspace; without one the schedule is whole tiles.
     Schedule s = make_schedule<Cfg>(g, g.workspace != nullptr);
     if (s.sk_ctas > 0 && g.workspace_bytes < workspace_bytes<Cfg>(s)) s = make_schedule<Cfg>(g, false);
-    if (s.sk_ctas > 0) {
-        const size_t flag_bytes =
-            round_up_bytes((size_t)s.sk_ctas * Cfg::CONSUMERS * sizeof(unsigned), kFlagBytesAlign);
-        s.flags = static_cast<unsigned *>(g.workspace);
-        s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(g.workspace) + flag_bytes);
-        e = cudaMemsetAsync(s.flags, 0, flag_bytes, stream);
-        if (e != cudaSuccess) return e;
-    }
+    if (s.sk_ctas > 0 && (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, stream)) != cudaSuccess)
+        return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
     float *C = g.C;
     int64_t ldc = g.ldc;

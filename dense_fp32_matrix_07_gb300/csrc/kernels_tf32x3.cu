@@ -15,7 +15,8 @@
 // into scratch; the product kernel then streams 128 x 16 and 256 x 16 tiles
 // of all four through TMA (64-byte swizzle) into a 4-stage ring.
 //
-// Product kernel: persistent, one 128 x 256 output tile at a time per CTA.
+// Product kernel: persistent, one 128 x 256 output tile (or a K-slab range of
+// one, under the stream-K tail of schedule.cuh) at a time per CTA.
 //   warp 0      TMA producer (one thread): 4 boxes per K slab, full/empty
 //               mbarriers per stage;
 //   warp 1      MMA issuer (one thread) and TMEM owner: per K slab of 16,
@@ -23,7 +24,10 @@
 //               TMEM accumulator; tcgen05.commit frees the stage, and at the
 //               end of a tile signals the epilogue;
 //   warps 4-7   epilogue: warp 4+q reads TMEM lanes 32q..32q+31 (rows of the
-//               tile) with tcgen05.ld and stores them to C.
+//               tile) with tcgen05.ld and stores them to C — or, for a
+//               slab range that does not start a tile, to this CTA's partial
+//               slot (then releases its flag); a tile's owner first adds the
+//               later CTAs' partials, in CTA order.
 // The accumulator is double-buffered (2 x 256 of the 512 TMEM columns), so
 // the epilogue of one tile overlaps the MMAs of the next. Every wait is
 // bounded in time; a role that gives up sets the device error word and skips
@@ -32,6 +36,7 @@
 #include "common.cuh"
 #include "configs.cuh"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -40,8 +45,9 @@ namespace sgemm_gb300 {
 
 namespace {
 
+template <int BN_, int STAGES_>
 struct Tf32x3Cfg {
-    static constexpr int BM = 128, BN = 256, BK = 16, STAGES = 4;
+    static constexpr int BM = 128, BN = BN_, BK = 16, STAGES = STAGES_;
     static constexpr int ROW_BYTES = BK * 4;                   // 64: 64-byte swizzle
     static constexpr int A_TILE = BM * ROW_BYTES;              // 8 KB
     static constexpr int B_TILE = BN * ROW_BYTES;              // 16 KB
@@ -56,25 +62,13 @@ struct Tf32x3Cfg {
     static_assert(TMEM_COLS <= 512, "tensor memory columns");
 };
 
-__device__ __forceinline__ void tile_coords_g8(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
-{
-    constexpr int GR = 8;
-    const int64_t per_group = (int64_t)GR * tiles_n;
-    const int64_t group = t / per_group;
-    const int first_m = (int)(group * GR);
-    const int rows = min(tiles_m - first_m, GR);
-    const int64_t local = t - group * per_group;
-    tm = first_m + (int)(local % rows);
-    tn = (int)(local / rows);
-}
-
-template <bool VEC_C>
-__global__ void __launch_bounds__(Tf32x3Cfg::THREADS, 1)
+template <class Cfg, bool VEC_C>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
 sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_constant__ CUtensorMap mapAlo,
                     const __grid_constant__ CUtensorMap mapBhi, const __grid_constant__ CUtensorMap mapBlo,
-                    float *__restrict__ C, int64_t ldc, int M, int N, int K, unsigned int *status)
+                    float *__restrict__ C, int64_t ldc, int M, int N, const Schedule sched,
+                    unsigned int *status)
 {
-    using Cfg = Tf32x3Cfg;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -93,9 +87,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
     uint32_t *tmem_slot_ptr = reinterpret_cast<uint32_t *>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int64_t tiles = (int64_t)tiles_m * tiles_n;
-    const int nk = (K + BK - 1) / BK;
+    const int g = blockIdx.x;
+    const int nk = sched.nk;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -128,10 +121,12 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
         for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        Cursor cur = cursor_init(sched, g);
+        Item item;
+        while (ok && next_item(sched, cur, item)) {
             int tm, tn;
-            tile_coords_g8(t, tiles_m, tiles_n, tm, tn);
-            for (int kb = 0; kb < nk; ++kb, ++it) {
+            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+            for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
                 const int s = (int)(it % STAGES);
                 const int round = (int)(it / STAGES);
                 if (!ptx::wait_phase(empty_bar(s), (round & 1) ^ 1)) {
@@ -158,7 +153,9 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             uint32_t it = 0, lt = 0;
-            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+            Cursor cur = cursor_init(sched, g);
+            Item item;
+            for (; next_item(sched, cur, item); ++lt) {
                 const int b = (int)(lt & 1);
                 const uint32_t use = lt >> 1;
                 if (!ptx::wait_phase(acce_bar(b), (use & 1) ^ 1)) {
@@ -168,7 +165,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                 ptx::tc_fence_after();
                 const uint32_t d = taddr + (uint32_t)(b * BN);
                 bool ok = true;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
                     const int s = (int)(it % STAGES);
                     if (!ptx::wait_phase(full_bar(s), (it / STAGES) & 1)) {
                         atomicOr(status, kStatusTimeout);
@@ -182,7 +179,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                         const uint64_t al = ptx::sdesc_kmajor(stage_a_lo(s) + ks * 32, Cfg::ROW_BYTES);
                         const uint64_t bh = ptx::sdesc_kmajor(stage_b_hi(s) + ks * 32, Cfg::ROW_BYTES);
                         const uint64_t bl = ptx::sdesc_kmajor(stage_b_lo(s) + ks * 32, Cfg::ROW_BYTES);
-                        ptx::mma_tf32(d, ah, bh, Cfg::IDESC, (kb | ks) ? 1u : 0u);
+                        ptx::mma_tf32(d, ah, bh, Cfg::IDESC, (kb != item.kb0 || ks != 0) ? 1u : 0u);
                         ptx::mma_tf32(d, ah, bl, Cfg::IDESC, 1u);
                         ptx::mma_tf32(d, al, bh, Cfg::IDESC, 1u);
                     }
@@ -199,8 +196,11 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
     } else {
         // ------------------------------ epilogue ------------------------------
         const int q = warp - Cfg::EPI_WARP0;          // TMEM lane quarter (== warp % 4)
+        const int et = 32 * q + lane;                 // epilogue thread: row of the tile
         uint32_t lt = 0;
-        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+        Cursor cur = cursor_init(sched, g);
+        Item item;
+        for (; next_item(sched, cur, item); ++lt) {
             const int b = (int)(lt & 1);
             const uint32_t use = lt >> 1;
             if (!ptx::wait_phase_warp(accf_bar(b), use & 1)) {
@@ -209,8 +209,24 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
             }
             ptx::tc_fence_after();
             int tm, tn;
-            tile_coords_g8(t, tiles_m, tiles_n, tm, tn);
-            const int64_t row = (int64_t)tm * BM + 32 * q + lane;
+            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+            const bool partial = item.kb0 > 0;                  // slabs of a tile owned earlier
+            const bool owner = item.kb0 == 0 && item.kb1 < nk;  // adds later CTAs' partials
+            int h_end = g + 1;
+            if (owner) {
+                const int64_t tile_end = (item.tile - sched.dp_tiles + 1) * nk;
+                while (h_end < sched.sk_ctas && sk_start(sched, h_end) < tile_end) ++h_end;
+                bool ok = true;
+                for (int h = g + 1; h < h_end && ok; ++h)
+                    ok = __all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)h * 4 + q)) != 0;
+                if (!ok) {
+                    if (lane == 0) atomicOr(status, kStatusTimeout);
+                    break;
+                }
+            }
+            // Partial-sum slot layout: float4 v (columns 4v..4v+3) of tile row
+            // et at index v * 128 + et, so each warp's accesses are coalesced.
+            const int64_t row = (int64_t)tm * BM + et;
             float *crow = C + row * ldc;
             const int col_base = tn * BN;
 #pragma unroll 1
@@ -224,20 +240,44 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce_bar(b));
                 }
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                if (partial) {
+                    float4 *slot = reinterpret_cast<float4 *>(sched.partials + (int64_t)g * BM * BN);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        slot[((c0 + j) / 4) * 128 + et] = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                    continue;
+                }
+                for (int h = g + 1; h < h_end; ++h) {
+                    const float4 *slot = reinterpret_cast<const float4 *>(sched.partials + (int64_t)h * BM * BN);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 p4 = slot[((c0 + j) / 4) * 128 + et];
+                        f[j] += p4.x;
+                        f[j + 1] += p4.y;
+                        f[j + 2] += p4.z;
+                        f[j + 3] += p4.w;
+                    }
+                }
                 if (row < M) {
                     const int col0 = col_base + c0;
                     if (VEC_C && col0 + 32 <= N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(crow + col0 + j) =
-                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                            if (col0 + j < N) crow[col0 + j] = f[j];
                     }
                 }
+            }
+            if (partial) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(sched.flags + (int64_t)g * 4 + q, 1u);
             }
         }
         ptx::tc_fence_before();
@@ -317,7 +357,8 @@ Tf32x3Layout tf32x3_layout(const GemmArgs &g)
     return l;
 }
 
-cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int64_t k, int64_t ld, int box_rows)
+cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int64_t k, int64_t ld, int box_rows,
+                          int box_k)
 {
     void *fnp = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -327,7 +368,7 @@ cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int6
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fnp);
     const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)Tf32x3Cfg::BK, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
                               box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -335,20 +376,33 @@ cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
+using Tf32x3Wide = Tf32x3Cfg<256, 4>;    // 128 x 256 tiles, 4 stages of 48 KB
+using Tf32x3Square = Tf32x3Cfg<128, 6>;  // 128 x 128 tiles, 6 stages of 32 KB
 
-size_t tf32x3_workspace_bytes(const GemmArgs &g) { return tf32x3_layout(g).total; }
-
-cudaError_t prepare_tf32x3()
+template <class Cfg>
+Schedule tf32x3_schedule(const GemmArgs &g, bool with_sk)
 {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_tf32x3_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Tf32x3Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sgemm_tf32x3_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Tf32x3Cfg::SMEM_BYTES);
+    return plan_schedule(g.M, g.N, g.K, Cfg::BM, Cfg::BN, Cfg::BK, g.num_sms, g.sched, with_sk);
 }
 
-cudaError_t launch_tf32x3(const GemmArgs &g, cudaStream_t stream)
+template <class Cfg>
+size_t tf32x3_workspace(const GemmArgs &g)
+{
+    return tf32x3_layout(g).total + schedule_workspace_bytes(tf32x3_schedule<Cfg>(g, true), 4, Cfg::BM, Cfg::BN);
+}
+
+template <class Cfg>
+cudaError_t prepare_cfg()
+{
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tf32x3_kernel<Cfg, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tf32x3_kernel<Cfg, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::SMEM_BYTES);
+}
+
+template <class Cfg>
+cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
 {
     const Tf32x3Layout l = tf32x3_layout(g);
     if (!g.workspace || g.workspace_bytes < l.total) return cudaErrorInvalidValue;
@@ -357,39 +411,67 @@ cudaError_t launch_tf32x3(const GemmArgs &g, cudaStream_t stream)
     float *a_lo = reinterpret_cast<float *>(ws + l.a_bytes);
     float *b_hi = reinterpret_cast<float *>(ws + 2 * l.a_bytes);
     float *b_lo = reinterpret_cast<float *>(ws + 2 * l.a_bytes + l.b_bytes);
+    cudaError_t e;
 
-    // Split pre-passes.
+    // Split pre-passes: A row by row; B transposed to K-major.
     {
         const int64_t gy = g.M < 65535 ? g.M : 65535;
         int64_t gx = (g.K + 255) / 256;
         if (gx > 64) gx = 64;
         tf32_split_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(g.A, g.M, g.K, g.lda, a_hi,
                                                                                    a_lo, l.kp);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int64_t tiles = ((g.K + 31) / 32) * ((g.N + 31) / 32);
         const unsigned grid = (unsigned)(tiles < (int64_t)g.num_sms * 32 ? tiles : (int64_t)g.num_sms * 32);
         tf32_split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(g.B, g.K, g.N, g.ldb, b_hi, b_lo, l.kp);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
 
     CUtensorMap mAh, mAl, mBh, mBl;
-    cudaError_t e;
-    if ((e = encode_kmajor(&mAh, a_hi, g.M, g.K, l.kp, Tf32x3Cfg::BM)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(&mAl, a_lo, g.M, g.K, l.kp, Tf32x3Cfg::BM)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Tf32x3Cfg::BN)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Tf32x3Cfg::BN)) != cudaSuccess) return e;
-    const int64_t tiles = ((g.M + Tf32x3Cfg::BM - 1) / Tf32x3Cfg::BM) * ((g.N + Tf32x3Cfg::BN - 1) / Tf32x3Cfg::BN);
-    const unsigned grid = (unsigned)(tiles < g.num_sms ? tiles : g.num_sms);
+    if ((e = encode_kmajor(&mAh, a_hi, g.M, g.K, l.kp, Cfg::BM, Cfg::BK)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mAl, a_lo, g.M, g.K, l.kp, Cfg::BM, Cfg::BK)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Cfg::BN, Cfg::BK)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Cfg::BN, Cfg::BK)) != cudaSuccess) return e;
+
+    // Stream-K partials and flags follow the split operands in the workspace.
+    Schedule sched = tf32x3_schedule<Cfg>(g, true);
+    if (sched.sk_ctas > 0 && g.workspace_bytes < l.total + schedule_workspace_bytes(sched, 4, Cfg::BM, Cfg::BN))
+        sched = tf32x3_schedule<Cfg>(g, false);
+    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, 4, stream)) != cudaSuccess)
+        return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
-    if (vec)
-        sgemm_tf32x3_kernel<true><<<grid, Tf32x3Cfg::THREADS, Tf32x3Cfg::SMEM_BYTES, stream>>>(
-            mAh, mAl, mBh, mBl, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+    float *C = g.C;
+    int64_t ldc = g.ldc;
+    int M = (int)g.M, N = (int)g.N;
+    unsigned int *status = g.status;
+    void *args[] = {&mAh, &mAl, &mBh, &mBl, &C, &ldc, &M, &N, &sched, &status};
+    const void *fn = vec ? reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, true>)
+                         : reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, false>);
+    // Owners wait on other CTAs' partial sums: all CTAs must be resident.
+    if (sched.sk_ctas > 1)
+        e = cudaLaunchCooperativeKernel(fn, dim3(sched.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
     else
-        sgemm_tf32x3_kernel<false><<<grid, Tf32x3Cfg::THREADS, Tf32x3Cfg::SMEM_BYTES, stream>>>(
-            mAh, mAl, mBh, mBl, g.C, g.ldc, (int)g.M, (int)g.N, (int)g.K, g.status);
+        e = cudaLaunchKernel(fn, dim3(sched.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tf32x3_workspace_bytes(int kernel, const GemmArgs &g)
+{
+    return kernel == kKernTf32x3_128x128 ? tf32x3_workspace<Tf32x3Square>(g) : tf32x3_workspace<Tf32x3Wide>(g);
+}
+
+cudaError_t prepare_tf32x3()
+{
+    const cudaError_t e = prepare_cfg<Tf32x3Wide>();
+    return e != cudaSuccess ? e : prepare_cfg<Tf32x3Square>();
+}
+
+cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream)
+{
+    return kernel == kKernTf32x3_128x128 ? launch_cfg<Tf32x3Square>(g, stream) : launch_cfg<Tf32x3Wide>(g, stream);
 }
 
 }  // namespace sgemm_gb300

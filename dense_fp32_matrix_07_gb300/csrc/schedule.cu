@@ -1,0 +1,61 @@
+// Host side of the shared work schedule (see schedule.cuh).
+#include "schedule.cuh"
+
+namespace sgemm_gb300 {
+
+namespace {
+size_t round_up_bytes(size_t x, size_t a) { return (x + a - 1) / a * a; }
+size_t flag_bytes(const Schedule &s, int flags_per_cta)
+{
+    return round_up_bytes((size_t)s.sk_ctas * flags_per_cta * sizeof(unsigned), 256);
+}
+}  // namespace
+
+Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
+                       bool with_sk)
+{
+    Schedule s{};
+    s.tiles_m = (int)((M + bm - 1) / bm);
+    s.tiles_n = (int)((N + bn - 1) / bn);
+    s.nk = (int)((K + bk - 1) / bk);
+    s.tiles = (int64_t)s.tiles_m * s.tiles_n;
+    s.dp_tiles = s.tiles;
+    s.sk_iters = 0;
+    s.sk_ctas = 0;
+    s.grid = (int)(s.tiles < slots ? s.tiles : slots);
+    bool sk = false;
+    if (with_sk && policy == kSchedStreamK) {
+        sk = true;
+    } else if (with_sk && policy == kSchedAuto) {
+        const int64_t rounds = (s.tiles + slots - 1) / slots;
+        sk = (double)s.tiles < 0.97 * (double)(rounds * slots) && s.nk >= 8;
+    }
+    if (!sk) return s;
+    const int64_t full_rounds = s.tiles / slots;
+    const int64_t dp_rounds = (policy == kSchedStreamK || full_rounds < 1) ? 0 : full_rounds - 1;
+    s.dp_tiles = dp_rounds * slots;
+    s.sk_iters = (s.tiles - s.dp_tiles) * s.nk;
+    const int64_t min_iters = policy == kSchedStreamK ? 1 : 4;
+    int64_t ctas = s.sk_iters / min_iters;
+    if (ctas > slots) ctas = slots;
+    if (ctas < 1) ctas = 1;
+    s.sk_ctas = (int)ctas;
+    s.grid = (int)(s.dp_tiles > 0 ? slots : ctas);
+    return s;
+}
+
+size_t schedule_workspace_bytes(const Schedule &s, int flags_per_cta, int bm, int bn)
+{
+    if (s.sk_ctas == 0) return 0;
+    return flag_bytes(s, flags_per_cta) + (size_t)s.sk_ctas * bm * bn * sizeof(float);
+}
+
+cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int flags_per_cta, cudaStream_t stream)
+{
+    const size_t fb = flag_bytes(s, flags_per_cta);
+    s.flags = static_cast<unsigned *>(workspace);
+    s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + fb);
+    return cudaMemsetAsync(s.flags, 0, fb, stream);
+}
+
+}  // namespace sgemm_gb300
