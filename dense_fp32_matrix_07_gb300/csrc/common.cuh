@@ -10,7 +10,9 @@ namespace sgemm_gb300 {
 enum SchedPolicy : int {
     kSchedAuto = 0,          // whole tiles, or stream-K when the last wave is short
     kSchedDataParallel = 1,  // whole tiles only (needs no workspace)
-    kSchedStreamK = 2        // every tile's K slabs shared out evenly (tests)
+    kSchedStreamK = 2,       // every tile's K slabs shared out evenly (tests)
+    kSchedTailSplit = 3      // whole tiles for full waves; each leftover tile
+                             // split into equal K parts that run in lockstep
 };
 
 // Arguments of one product C = A . B (row-major, FP32, device pointers).

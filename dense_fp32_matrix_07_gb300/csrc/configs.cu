@@ -18,10 +18,11 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"ladder_coalesced", kKernLadderCoalesced, kSchedDataParallel, false, false, 16, 16},
     {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, false, 128, 128},
     {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, false, 16, 16},
-    {"tf32x3_128x256_k16_s4", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
+    {"tf32x3_128x256_k16_s4", kKernTf32x3_128x256, kSchedTailSplit, true, false, 128, 256},
     {"tf32x3_128x256_k16_s4_sk", kKernTf32x3_128x256, kSchedStreamK, true, false, 128, 256},
     {"tf32x3_128x256_k16_s4_auto", kKernTf32x3_128x256, kSchedAuto, true, false, 128, 256},
     {"tf32x3_128x128_k16_s6", kKernTf32x3_128x128, kSchedDataParallel, true, false, 128, 128},
+    {"tf32x3_128x256_k16_s4_dp", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)

@@ -54,6 +54,7 @@ enum ConfigId : int {
     kCfgTf32x3_128x256_sk,
     kCfgTf32x3_128x256_auto,
     kCfgTf32x3_128x128,
+    kCfgTf32x3_128x256_dp,
     kNumConfigs
 };
 

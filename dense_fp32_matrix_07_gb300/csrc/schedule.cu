@@ -23,6 +23,21 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
     s.sk_iters = 0;
     s.sk_ctas = 0;
     s.grid = (int)(s.tiles < slots ? s.tiles : slots);
+    if (with_sk && policy == kSchedTailSplit) {
+        // Leftover tiles of the last, partial wave are each cut into `parts`
+        // equal K ranges, one per CTA: the ranges start together at aligned
+        // K offsets, so the tail runs as `parts` lockstep fronts.
+        const int64_t full_rounds = s.tiles / slots;
+        const int64_t rem = s.tiles - full_rounds * slots;
+        const int64_t parts = rem > 0 ? slots / rem : 0;
+        if (parts >= 2 && s.nk >= 2 * parts) {
+            s.dp_tiles = full_rounds * slots;
+            s.sk_iters = rem * s.nk;
+            s.sk_ctas = (int)(rem * parts);
+            s.grid = (int)(s.dp_tiles > 0 ? slots : s.sk_ctas);
+        }
+        return s;
+    }
     bool sk = false;
     if (with_sk && policy == kSchedStreamK) {
         sk = true;

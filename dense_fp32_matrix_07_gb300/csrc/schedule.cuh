@@ -121,10 +121,12 @@ __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n,
 
 // Plans the schedule of an M x N x K product in bm x bn tiles with bk-deep
 // slabs on `slots` resident CTAs. Policy (SchedPolicy): whole tiles; forced
-// stream-K over every tile, split down to one slab per CTA (for tests); or
+// stream-K over every tile, split down to one slab per CTA (for tests);
 // automatic: stream-K only when whole tiles would leave the last wave below
 // 97 % full and a tile spans at least 8 slabs, keeping at least 4 slabs per
-// CTA. `with_sk` false always gives whole tiles. Pointers are left null.
+// CTA; or tail split: whole tiles for every full wave, then each leftover
+// tile cut into floor(slots / leftover) >= 2 equal K parts. `with_sk` false
+// always gives whole tiles. Pointers are left null.
 Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
                        bool with_sk);
 
