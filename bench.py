@@ -50,7 +50,7 @@ DEFAULT_SM_MAX_MHZ = 2070.0      # GB300 maximum SM clock
 L2_BYTES = 126.5 * 2 ** 20       # GB300 L2 capacity
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffma_tma_sq4096.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_07_gb300", "csrc", f)
-                  for f in ("kernels_ffma_tma.cu", "ptx.cuh")]
+                  for f in ("kernels_ffma_tma.cu", "ptx.cuh", "schedule.cuh", "schedule.cu")]
 
 
 def product_flops(M: int, N: int, K: int) -> float:
