@@ -70,6 +70,10 @@ def load_library(path: str):
     lib.oracle_sgemm_rows_f64.restype = ctypes.c_int
     lib.oracle_sgemm_rows_f64.argtypes = [_i64, _i64, _i64, _fp, _i64, _fp, _i64,
                                           _lp, _i64, _dp, _dp]
+    lib.oracle_sgemm_general_f64.restype = ctypes.c_int
+    lib.oracle_sgemm_general_f64.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_double,
+                                             _fp, _i64, _i64, _fp, _i64, _i64,
+                                             ctypes.c_double, _fp, _i64, _i64, _i64, _dp, _dp]
     lib.oracle_sgemm_cols_f64.restype = ctypes.c_int
     lib.oracle_sgemm_cols_f64.argtypes = [_i64, _i64, _i64, _fp, _i64, _fp, _i64,
                                           _lp, _i64, _dp, _dp]
@@ -169,9 +173,32 @@ class Oracle:
         return C, S
 
 
+    def sgemm_general(self, op_a, op_b, M, N, K, alpha, A, lda, sa, B, ldb, sb,
+                      beta, Cin, ldc, sc, batch, want_abs=True):
+        """alpha * op(A_b) . op(B_b) + beta * C_b for b < batch. A, B, Cin:
+        flat float32 arrays (Cin may be None when beta == 0). Returns (C, S)
+        as float64 (batch, M, N) arrays."""
+        A = np.ascontiguousarray(np.asarray(A, dtype=np.float32).reshape(-1))
+        B = np.ascontiguousarray(np.asarray(B, dtype=np.float32).reshape(-1))
+        Cp = None
+        if Cin is not None:
+            Cp = np.ascontiguousarray(np.asarray(Cin, dtype=np.float32).reshape(-1))
+        C = np.empty((batch, M, N), dtype=np.float64)
+        S = np.empty((batch, M, N), dtype=np.float64) if want_abs else None
+        rc = self.lib.oracle_sgemm_general_f64(op_a, op_b, M, N, K, float(alpha),
+                                               self._ptr(A, _fp), lda, sa, self._ptr(B, _fp), ldb, sb,
+                                               float(beta), self._ptr(Cp, _fp) if Cp is not None else None,
+                                               ldc, sc, batch, self._ptr(C, _dp),
+                                               self._ptr(S, _dp) if S is not None else None)
+        if rc != 0:
+            raise ValueError(f"oracle_sgemm_general_f64 rejected its arguments ({rc})")
+        return C, S
+
+
 _default = Oracle()
 sgemm = _default.sgemm
 sgemm_rows = _default.sgemm_rows
 sgemm_cols = _default.sgemm_cols
+sgemm_general = _default.sgemm_general
 num_threads = _default.num_threads
 set_num_threads = _default.set_num_threads

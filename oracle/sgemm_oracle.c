@@ -163,3 +163,58 @@ int oracle_sgemm_cols_f64(int64_t M, int64_t N, int64_t K,
     free(Bsel);
     return 0;
 }
+
+/*
+ * General form (a library extension of the definition above; the pages have
+ * no alpha, beta, transposes or batches):
+ *
+ *   C_b[i][j] = alpha * sum_k opA_b[i][k] * opB_b[k][j] + beta * C_b[i][j]
+ *
+ * for b in [0, batch), i < M, j < N, where opA_b[i][k] = A[b*sa + i*lda + k]
+ * (op_a == 0, A stored M x K) or A[b*sa + k*lda + i] (op_a == 1, A stored
+ * K x M), and opB_b[k][j] = B[b*sb + k*ldb + j] (op_b == 0) or
+ * B[b*sb + j*ldb + k] (op_b == 1). C_in (float, leading dimension ldc, batch
+ * stride sc) is read only when beta != 0. Results go to Cout (double, M x N
+ * per batch entry, contiguous); S (nullable, same shape) receives
+ * |alpha| * sum_k |opA opB| + |beta * C_in|, the scale of the tolerance.
+ * Plain triple loop per entry in i, k, j order.
+ */
+int oracle_sgemm_general_f64(int op_a, int op_b, int64_t M, int64_t N, int64_t K, double alpha,
+                             const float *A, int64_t lda, int64_t sa,
+                             const float *B, int64_t ldb, int64_t sb,
+                             double beta, const float *Cin, int64_t ldc, int64_t sc,
+                             int64_t batch, double *Cout, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return -1;
+    if ((op_a != 0 && op_a != 1) || (op_b != 0 && op_b != 1)) return -1;
+    if (batch == 0 || M == 0 || N == 0) return 0;
+    if (beta != 0.0 && (!Cin || ldc < N)) return -1;
+    if (K > 0 && (!A || !B)) return -1;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t i = 0; i < M; ++i) {
+            double *crow = Cout + (b * M + i) * N;
+            double *srow = S ? S + (b * M + i) * N : NULL;
+            for (int64_t j = 0; j < N; ++j) {
+                crow[j] = 0.0;
+                if (srow) srow[j] = 0.0;
+            }
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = (double)(op_a == 0 ? A[b * sa + i * lda + k] : A[b * sa + k * lda + i]);
+                for (int64_t j = 0; j < N; ++j) {
+                    const double bv = (double)(op_b == 0 ? B[b * sb + k * ldb + j] : B[b * sb + j * ldb + k]);
+                    const double p = a * bv;
+                    crow[j] += p;
+                    if (srow) srow[j] += fabs(p);
+                }
+            }
+            for (int64_t j = 0; j < N; ++j) {
+                const double c = beta != 0.0 ? (double)Cin[b * sc + i * ldc + j] : 0.0;
+                crow[j] = alpha * crow[j] + beta * c;
+                if (srow) srow[j] = fabs(alpha) * srow[j] + fabs(beta * c);
+            }
+        }
+    }
+    return 0;
+}

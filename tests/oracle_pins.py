@@ -191,6 +191,88 @@ def check_special_values(o):
     assert Ce.shape == (0, 4)
 
 
+def check_general_reduces_to_plain(o):
+    """op = (as stored, as stored), alpha = 1, beta = 0, one entry: the
+    general form is the plain product, bit for bit."""
+    M, N, K = 23, 19, 37
+    A, B = _pair(M, N, K, "normal", 31)
+    C, S = o.sgemm(M, N, K, A, K, B, N)
+    G, GS = o.sgemm_general(0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, None, N, 0, 1)
+    assert np.array_equal(G[0], C) and np.array_equal(GS[0], S)
+
+
+def check_general_transposes(o):
+    """A stored transposed (K x M) with op_a = 1, B stored transposed (N x K)
+    with op_b = 1, each give the same product as the plain layout."""
+    M, N, K = 13, 17, 29
+    A, B = _pair(M, N, K, "normal", 32)
+    C, _ = o.sgemm(M, N, K, A, K, B, N)
+    At, Bt = np.ascontiguousarray(A.T), np.ascontiguousarray(B.T)
+    for op_a, op_b, a, lda, b, ldb in ((1, 0, At, M, B, N), (0, 1, A, K, Bt, K), (1, 1, At, M, Bt, K)):
+        G, _ = o.sgemm_general(op_a, op_b, M, N, K, 1.0, a, lda, 0, b, ldb, 0, 0.0, None, N, 0, 1)
+        assert np.array_equal(G[0], C), (op_a, op_b)
+
+
+def check_general_alpha_beta(o):
+    """All-ones A and B (C = K), times alpha, plus beta * C_in, exactly; beta
+    = 0 never reads C_in (NaN there stays out)."""
+    M, N, K = 5, 6, 7
+    A = np.ones(M * K, np.float32)
+    B = np.ones(K * N, np.float32)
+    Cin = (np.arange(M * N, dtype=np.float32) - 9).reshape(M, N)
+    for alpha, beta in ((2.0, 0.0), (-0.5, 3.0), (0.0, -1.0), (1.0, 1.0)):
+        G, S = o.sgemm_general(0, 0, M, N, K, alpha, A, K, 0, B, N, 0, beta, Cin, N, 0, 1)
+        want = alpha * K + beta * Cin.astype(np.float64)
+        assert np.array_equal(G[0], want), (alpha, beta)
+        assert np.array_equal(S[0], abs(alpha) * K + np.abs(beta * Cin.astype(np.float64))), (alpha, beta)
+    nan_c = np.full((M, N), np.nan, np.float32)
+    G, _ = o.sgemm_general(0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, nan_c, N, 0, 1)
+    assert not np.isnan(G).any()
+
+
+def check_general_batch(o):
+    """Entry b of a strided batch equals the plain product of entry b;
+    stride 0 shares one operand across the batch."""
+    M, N, K, batch = 9, 11, 14, 4
+    sa, sb, sc = M * K + 3, K * N + 5, M * N + 2
+    rng = np.random.default_rng(33)
+    A = rng.standard_normal(batch * sa).astype(np.float32)
+    B = rng.standard_normal(batch * sb).astype(np.float32)
+    Cin = rng.standard_normal(batch * sc).astype(np.float32)
+    G, _ = o.sgemm_general(0, 0, M, N, K, 1.5, A, K, sa, B, N, sb, -2.0, Cin, N, sc, batch)
+    Gs, _ = o.sgemm_general(0, 0, M, N, K, 1.0, A, K, sa, B, N, 0, 0.0, None, N, 0, batch)
+    for b in range(batch):
+        C, _ = o.sgemm(M, N, K, A[b * sa:], K, B[b * sb:], N)
+        cin = Cin[b * sc: b * sc + M * N].reshape(M, N).astype(np.float64)
+        assert np.array_equal(G[b], 1.5 * C - 2.0 * cin), b
+        C0, _ = o.sgemm(M, N, K, A[b * sa:], K, B, N)
+        assert np.array_equal(Gs[b], C0), b
+
+
+def check_general_bruteforce_rational(o, seed=34):
+    """Tiny shapes, both ops, alpha and beta: within the double rounding bound
+    of the exact rational result."""
+    rng = np.random.default_rng(seed)
+    for M, N, K in itertools.product((1, 2, 3), (1, 3), (1, 2, 4)):
+        for op_a, op_b in itertools.product((0, 1), repeat=2):
+            alpha, beta = float(rng.choice([0.5, -3.0, 1.25])), float(rng.choice([0.0, 2.0, -0.75]))
+            Ar = rng.standard_normal((K, M) if op_a else (M, K)).astype(np.float32)
+            Br = rng.standard_normal((N, K) if op_b else (K, N)).astype(np.float32)
+            Cin = rng.standard_normal((M, N)).astype(np.float32)
+            G, S = o.sgemm_general(op_a, op_b, M, N, K, alpha, Ar, Ar.shape[1], 0, Br, Br.shape[1], 0,
+                                   beta, Cin, N, 0, 1)
+            for i in range(M):
+                for j in range(N):
+                    acc = sum(Fraction(float(Ar[k, i] if op_a else Ar[i, k])) *
+                              Fraction(float(Br[j, k] if op_b else Br[k, j])) for k in range(K))
+                    sab = sum(abs(Fraction(float(Ar[k, i] if op_a else Ar[i, k])) *
+                                  Fraction(float(Br[j, k] if op_b else Br[k, j]))) for k in range(K))
+                    exact = Fraction(alpha) * acc + Fraction(beta) * Fraction(float(Cin[i, j]))
+                    scale = abs(Fraction(alpha)) * sab + abs(Fraction(beta) * Fraction(float(Cin[i, j])))
+                    bound = Fraction(K + 3, 2 ** 52) * scale
+                    assert abs(Fraction(float(G[0, i, j])) - exact) <= bound, (M, N, K, op_a, op_b, i, j)
+
+
 ALL_CHECKS = [
     check_bruteforce_rational,
     check_identity,
@@ -202,4 +284,9 @@ ALL_CHECKS = [
     check_transpose,
     check_abs_sum,
     check_special_values,
+    check_general_reduces_to_plain,
+    check_general_transposes,
+    check_general_alpha_beta,
+    check_general_batch,
+    check_general_bruteforce_rational,
 ]

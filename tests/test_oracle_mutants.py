@@ -20,20 +20,29 @@ SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "sgemm_oracle.c")
 MUTANTS = {
     "drop_last_k_term": ("for (int64_t k = 0; k < K; ++k) {\n        const double a",
                          "for (int64_t k = 0; k < K - 1; ++k) {\n        const double a"),
-    "wrong_sign": ("crow[j] += p;", "crow[j] -= p;"),
+    "wrong_sign": ("\n            crow[j] += p;", "\n            crow[j] -= p;"),
     "transposed_B": ("const double p = a * (double)brow[j];",
                      "const double p = a * (double)B[(j < K ? j : 0) * ldb + (k < N ? k : 0)];"),
     "ignores_lda": ("oracle_row(N, K, K > 0 ? A + i * lda : A,",
                     "oracle_row(N, K, K > 0 ? A + i * K : A,"),
     "ignores_ldb": ("const float *brow = B + k * ldb;", "const float *brow = B + k * N;"),
-    "no_init": ("crow[j] = 0.0;\n", "crow[j] = (j == 0) ? 1.0 : 0.0;\n"),
-    "float_accumulate": ("crow[j] += p;", "crow[j] = (float)(crow[j] + p);"),
+    "no_init": ("\n        crow[j] = 0.0;\n", "\n        crow[j] = (j == 0) ? 1.0 : 0.0;\n"),
+    "float_accumulate": ("\n            crow[j] += p;", "\n            crow[j] = (float)(crow[j] + p);"),
     "shifted_k_index": ("const double a = (double)arow[k];",
                         "const double a = (double)arow[k > 0 ? k - 1 : 0];"),
-    "abs_without_abs": ("srow[j] += fabs(p);", "srow[j] += p;"),
+    "abs_without_abs": ("\n            if (srow) srow[j] += fabs(p);", "\n            if (srow) srow[j] += p;"),
     "rows_wrong_index": ("oracle_row(N, K, A + rows[r] * lda,", "oracle_row(N, K, A + r * lda,"),
     "cols_wrong_index": ("Bsel[k * ncols + c] = B[k * ldb + cols[c]];",
                          "Bsel[k * ncols + c] = B[k * ldb + c];"),
+    "general_transposed_a_index": ("A[b * sa + i * lda + k] : A[b * sa + k * lda + i]",
+                                   "A[b * sa + i * lda + k] : A[b * sa + i * lda + k]"),
+    "general_transposed_b_index": ("B[b * sb + k * ldb + j] : B[b * sb + j * ldb + k]",
+                                   "B[b * sb + k * ldb + j] : B[b * sb + k * ldb + j]"),
+    "general_no_alpha": ("crow[j] = alpha * crow[j] + beta * c;", "crow[j] = crow[j] + beta * c;"),
+    "general_beta_sign": ("crow[j] = alpha * crow[j] + beta * c;", "crow[j] = alpha * crow[j] - beta * c;"),
+    "general_ignores_batch_stride_b": ("B[b * sb + k * ldb + j] :", "B[k * ldb + j] :"),
+    "general_abs_without_alpha": ("srow[j] = fabs(alpha) * srow[j] + fabs(beta * c);",
+                                  "srow[j] = srow[j] + fabs(beta * c);"),
 }
 
 
