@@ -31,7 +31,7 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
-            "sgemm_test_withhold_copy")
+            "sgemm_test_withhold_copy", "sgemm_general", "sgemm_general_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,12 @@ def load(rebuild: bool = False):
             lib.sgemm_test_withhold_copy.restype = ctypes.c_int
             lib.sgemm_test_withhold_copy.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
                                                      _i64, ctypes.c_int, _vp]
+            gen = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
+                   _vp, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _i64]
+            lib.sgemm_general.restype = ctypes.c_int
+            lib.sgemm_general.argtypes = gen + [_vp]
+            lib.sgemm_general_ex.restype = ctypes.c_int
+            lib.sgemm_general_ex.argtypes = gen + [ctypes.c_int, _vp]
             lib.sgemm_check_status.restype = ctypes.c_int
             lib.sgemm_check_status.argtypes = [_vp]
             lib.sgemm_error_string.restype = ctypes.c_char_p
@@ -110,6 +116,20 @@ def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) ->
     `slab`-th K slab, so the kernel's bounded waits expire (about a second)
     and sgemm_check_status() reports SGEMM_ERR_TIMEOUT."""
     return load().sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream)
+
+
+def sgemm_general(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                  beta, C, ldc, stride_c, batch, stream=0) -> int:
+    """C_b = alpha * op(A_b) . op(B_b) + beta * C_b for b < batch."""
+    return load().sgemm_general(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                                beta, C, ldc, stride_c, batch, stream)
+
+
+def sgemm_general_ex(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                     beta, C, ldc, stride_c, batch, config, stream=0) -> int:
+    """sgemm_general() with a forced kernel configuration (-1 = automatic)."""
+    return load().sgemm_general_ex(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                                   beta, C, ldc, stride_c, batch, config, stream)
 
 
 def sgemm_check_status(stream=0) -> int:

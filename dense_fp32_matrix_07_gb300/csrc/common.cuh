@@ -30,6 +30,15 @@ struct GemmArgs {
     void *workspace = nullptr;     // stream-K partial sums and flags, or null
     size_t workspace_bytes = 0;
     int withhold_it = -1;          // test hook: CTA 0's producer skips this copy
+    // General form: C_b = alpha * A_b . B_b + beta * C_b for b < batch, with
+    // batch strides in elements (a stride of 0 shares one operand).
+    float alpha = 1.0f, beta = 0.0f;
+    int64_t batch = 1;
+    int64_t stride_a = 0, stride_b = 0, stride_c = 0;
+    // Operand storage: 0 as multiplied (A: M x K, B: K x N), 1 transposed
+    // (A stored K x M, B stored N x K). Only kernels that read the operands
+    // themselves (the 3xTF32 split) see 1; the others get packed copies.
+    int op_a = 0, op_b = 0;
 };
 
 // Bits of the device error word.
@@ -52,6 +61,19 @@ cudaError_t launch_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc,
 cudaError_t launch_pack(const float *src, int64_t rows, int64_t cols,
                         int64_t ld_src, float *dst, int64_t ld_dst,
                         cudaStream_t stream);
+// Batched copies: entry b of src (rows x cols, ld_src, batch stride
+// s_src) to dst (ld_dst, batch stride s_dst); the transposing variant
+// writes dst[b][c][r] = src[b][r][c].
+cudaError_t launch_pack_batched(const float *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                int64_t s_src, float *dst, int64_t ld_dst, int64_t s_dst,
+                                int64_t batch, cudaStream_t stream);
+cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_t cols,
+                                          int64_t ld_src, int64_t s_src, float *dst,
+                                          int64_t ld_dst, int64_t s_dst, int64_t batch,
+                                          cudaStream_t stream);
+// C_b = beta * C_b (beta == 0 writes zeros without reading C).
+cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, int64_t stride_c,
+                         int64_t batch, float beta, cudaStream_t stream);
 cudaError_t launch_tiled_simple(const GemmArgs &g, cudaStream_t stream);
 
 }  // namespace sgemm_gb300

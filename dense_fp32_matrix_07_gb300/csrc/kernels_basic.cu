@@ -124,4 +124,112 @@ cudaError_t launch_pack(const float *src, int64_t rows, int64_t cols,
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Batched layout kernels of the general form alpha * op(A) . op(B) + beta * C.
+// ---------------------------------------------------------------------------
+
+// dst[b * s_dst + r * ld_dst + c] = src[b * s_src + r * ld_src + c].
+__global__ void pack_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
+                                    int64_t ld_src, int64_t s_src, float *__restrict__ dst,
+                                    int64_t ld_dst, int64_t s_dst, int64_t batch)
+{
+    const int64_t segs = (cols + 255) / 256;
+    const int64_t work = batch * rows * segs;
+    const int warps = blockDim.x / 32;
+    const int lane = threadIdx.x & 31;
+    for (int64_t w = blockIdx.x * (int64_t)warps + threadIdx.x / 32; w < work;
+         w += (int64_t)gridDim.x * warps) {
+        const int64_t seg = w % segs, rb = w / segs;
+        const int64_t r = rb % rows, b = rb / rows;
+        const float *sr = src + b * s_src + r * ld_src;
+        float *dr = dst + b * s_dst + r * ld_dst;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t c = seg * 256 + q * 32 + lane;
+            if (c < cols) dr[c] = sr[c];
+        }
+    }
+}
+
+// dst[b * s_dst + c * ld_dst + r] = src[b * s_src + r * ld_src + c], through
+// 32 x 32 shared-memory tiles so reads and writes are both coalesced.
+__global__ void pack_transpose_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
+                                              int64_t ld_src, int64_t s_src, float *__restrict__ dst,
+                                              int64_t ld_dst, int64_t s_dst, int64_t batch)
+{
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8 threads
+    const int64_t tiles_c = (cols + 31) / 32;
+    const int64_t per_entry = ((rows + 31) / 32) * tiles_c;
+    for (int64_t t = blockIdx.x; t < batch * per_entry; t += gridDim.x) {
+        const int64_t b = t / per_entry, tt = t % per_entry;
+        const int64_t r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
+        const float *sb = src + b * s_src;
+        float *db = dst + b * s_dst;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
+            tile[ty + 8 * i][tx] = (r < rows && c < cols) ? sb[r * ld_src + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;
+            if (c < cols && r < rows) db[c * ld_dst + r] = tile[tx][ty + 8 * i];
+        }
+        __syncthreads();
+    }
+}
+
+// C_b = beta * C_b; beta == 0 writes zeros without reading C.
+__global__ void scale_batched_kernel(float *__restrict__ C, int64_t M, int64_t N, int64_t ldc,
+                                     int64_t stride_c, int64_t batch, float beta)
+{
+    const int64_t total = batch * M * N;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = e % N, ib = e / N;
+        const int64_t i = ib % M, b = ib / M;
+        float *p = C + b * stride_c + i * ldc + j;
+        *p = beta != 0.0f ? beta * *p : 0.0f;
+    }
+}
+
+namespace {
+unsigned grid_for(int64_t work, int64_t per_block, int64_t cap)
+{
+    int64_t g = (work + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    return (unsigned)(g < cap ? g : cap);
+}
+}  // namespace
+
+cudaError_t launch_pack_batched(const float *src, int64_t rows, int64_t cols, int64_t ld_src,
+                                int64_t s_src, float *dst, int64_t ld_dst, int64_t s_dst,
+                                int64_t batch, cudaStream_t stream)
+{
+    pack_batched_kernel<<<grid_for(batch * rows * ((cols + 255) / 256), 8, 8192), 256, 0, stream>>>(
+        src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_t cols,
+                                          int64_t ld_src, int64_t s_src, float *dst,
+                                          int64_t ld_dst, int64_t s_dst, int64_t batch,
+                                          cudaStream_t stream)
+{
+    const int64_t tiles = batch * ((rows + 31) / 32) * ((cols + 31) / 32);
+    pack_transpose_batched_kernel<<<grid_for(tiles, 1, 8192), dim3(32, 8), 0, stream>>>(
+        src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale(float *C, int64_t M, int64_t N, int64_t ldc, int64_t stride_c,
+                         int64_t batch, float beta, cudaStream_t stream)
+{
+    scale_batched_kernel<<<grid_for(batch * M * N, 256, 4096), 256, 0, stream>>>(C, M, N, ldc, stride_c,
+                                                                               batch, beta);
+    return cudaGetLastError();
+}
+
 }  // namespace sgemm_gb300

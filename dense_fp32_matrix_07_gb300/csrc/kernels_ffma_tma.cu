@@ -102,13 +102,25 @@ struct FfmaTmaCfg {
                   "register split exceeds the launch allocation");
 };
 
+// Output side of a launch: C_b = alpha * acc + beta * C_b (C read only when
+// beta != 0) for batch entry b at C + b * stride_c; a_bz / b_bz are 1 when A
+// / B advance with the batch entry (their tensor maps' third coordinate)
+// and 0 when one operand is shared by every entry.
+struct Epilogue {
+    float *C;
+    int64_t ldc, stride_c;
+    int M, N;
+    float alpha, beta;
+    int a_bz, b_bz;
+};
+
 template <class Cfg, bool VEC_C>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapB,
-                      float *__restrict__ C, int64_t ldc, int M, int N,
-                      const Schedule sched, unsigned int *status, int withhold_it)
+                      const Epilogue ep, const Schedule sched, unsigned int *status, int withhold_it)
 {
+    const int M = ep.M, N = ep.N;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TN = Cfg::TN, G = Cfg::G;
     extern __shared__ uint8_t smem_raw[];
@@ -148,8 +160,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         Cursor cur = cursor_init(sched, g);
         Item item;
         while (ok && next_item(sched, cur, item)) {
-            int tm, tn;
-            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+            int bt, tm, tn;
+            tile_coords_b(sched, item.tile, bt, tm, tn);
             for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
                 const int s = (int)(it % STAGES);
                 const int round = (int)(it / STAGES);
@@ -162,8 +174,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                 // issued, so the consumers' wait for it must time out.
                 if (g == 0 && (int)it == withhold_it) continue;
                 ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
-                ptx::tma_load_2d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), kb * BK, tm * BM, policy);
-                ptx::tma_load_2d(sB + s * Cfg::B_BYTES, &mapB, full_bar(s), tn * BN, kb * BK, policy);
+                ptx::tma_load_3d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), kb * BK, tm * BM, bt * ep.a_bz,
+                                 policy);
+                ptx::tma_load_3d(sB + s * Cfg::B_BYTES, &mapB, full_bar(s), tn * BN, kb * BK, bt * ep.b_bz,
+                                 policy);
                 last_round[s] = round;
             }
         }
@@ -191,8 +205,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     Cursor cur = cursor_init(sched, g);
     Item item;
     while (next_item(sched, cur, item)) {
-        int tm, tn;
-        tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+        int bt, tm, tn;
+        tile_coords_b(sched, item.tile, bt, tm, tn);
 
         // acc[i][4q + e] holds C[row i][column group q, element e]; accp is
         // the same tile as FFMA2 pairs (e = 0,1 and e = 2,3).
@@ -309,17 +323,30 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int i = 0; i < 8; ++i) {
             const int64_t row = row0 + 8 * i;
             if (row >= M) break;
-            float *crow = C + row * ldc;
+            float *crow = ep.C + (int64_t)bt * ep.stride_c + row * ep.ldc;
 #pragma unroll
             for (int q = 0; q < G; ++q) {
                 const int col = col0 + 16 * q;
                 if (VEC_C && col + 3 < N) {
-                    *reinterpret_cast<float4 *>(crow + col) =
-                        make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
+                    float4 *p = reinterpret_cast<float4 *>(crow + col);
+                    float4 v = make_float4(ep.alpha * acc[i][4 * q], ep.alpha * acc[i][4 * q + 1],
+                                           ep.alpha * acc[i][4 * q + 2], ep.alpha * acc[i][4 * q + 3]);
+                    if (ep.beta != 0.0f) {
+                        const float4 o = *p;
+                        v.x = fmaf(ep.beta, o.x, v.x);
+                        v.y = fmaf(ep.beta, o.y, v.y);
+                        v.z = fmaf(ep.beta, o.z, v.z);
+                        v.w = fmaf(ep.beta, o.w, v.w);
+                    }
+                    *p = v;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (col + e < N) crow[col + e] = acc[i][4 * q + e];
+                        if (col + e < N) {
+                            float v = ep.alpha * acc[i][4 * q + e];
+                            if (ep.beta != 0.0f) v = fmaf(ep.beta, crow[col + e], v);
+                            crow[col + e] = v;
+                        }
                 }
             }
         }
@@ -352,19 +379,24 @@ cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
     return cudaSuccess;
 }
 
-// Row-major rows x cols FP32 matrix with leading dimension ld (elements),
-// read in boxes of box_rows x box_cols.
-cudaError_t encode_2d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
-                      int box_rows, int box_cols, CUtensorMapSwizzle swizzle)
+// A batch of `batch` row-major rows x cols FP32 matrices, leading dimension
+// ld and batch stride `stride` (elements), read in boxes of box_rows x
+// box_cols of one entry. batch 1 (or a shared operand) uses stride rows*ld.
+cudaError_t encode_3d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld,
+                      int64_t batch, int64_t stride, int box_rows, int box_cols, CUtensorMapSwizzle swizzle)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     const cudaError_t e = get_encoder(&encode);
     if (e != cudaSuccess) return e;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims,
+    if (batch <= 1) {
+        batch = 1;
+        stride = rows * ld;
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)stride * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims,
                               strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -385,7 +417,7 @@ template <class Cfg>
 Schedule make_schedule(const GemmArgs &g, bool with_sk)
 {
     return plan_schedule(g.M, g.N, g.K, Cfg::BM, Cfg::BN, Cfg::BK, g.num_sms * Cfg::MIN_BLOCKS, g.sched,
-                         with_sk);
+                         with_sk, g.batch);
 }
 
 template <class Cfg>
@@ -398,22 +430,26 @@ template <class Cfg>
 cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
 {
     CUtensorMap mapA, mapB;
-    cudaError_t e = encode_2d(&mapA, g.A, g.M, g.K, g.lda, Cfg::BM, Cfg::BK, Cfg::A_SWIZZLE);
+    // An operand with batch stride 0 is one matrix shared by every entry.
+    const int a_bz = (g.batch > 1 && g.stride_a != 0) ? 1 : 0;
+    const int b_bz = (g.batch > 1 && g.stride_b != 0) ? 1 : 0;
+    cudaError_t e = encode_3d(&mapA, g.A, g.M, g.K, g.lda, a_bz ? g.batch : 1, g.stride_a, Cfg::BM, Cfg::BK,
+                              Cfg::A_SWIZZLE);
     if (e != cudaSuccess) return e;
-    e = encode_2d(&mapB, g.B, g.K, g.N, g.ldb, Cfg::BK, Cfg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    e = encode_3d(&mapB, g.B, g.K, g.N, g.ldb, b_bz ? g.batch : 1, g.stride_b, Cfg::BK, Cfg::BN,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     // Stream-K needs the caller's workspace; without one the schedule is whole tiles.
     Schedule s = make_schedule<Cfg>(g, g.workspace != nullptr);
     if (s.sk_ctas > 0 && g.workspace_bytes < workspace_bytes<Cfg>(s)) s = make_schedule<Cfg>(g, false);
     if (s.sk_ctas > 0 && (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, stream)) != cudaSuccess)
         return e;
-    const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
-    float *C = g.C;
-    int64_t ldc = g.ldc;
-    int M = (int)g.M, N = (int)g.N;
+    const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0) &&
+                     (g.batch <= 1 || g.stride_c % 4 == 0);
+    Epilogue ep{g.C, g.ldc, g.batch > 1 ? g.stride_c : 0, (int)g.M, (int)g.N, g.alpha, g.beta, a_bz, b_bz};
     unsigned int *status = g.status;
     int withhold = g.withhold_it;
-    void *args[] = {&mapA, &mapB, &C, &ldc, &M, &N, &s, &status, &withhold};
+    void *args[] = {&mapA, &mapB, &ep, &s, &status, &withhold};
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false>);
     // Owners wait on other CTAs' partial sums: all CTAs must be resident.
@@ -454,6 +490,7 @@ size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
 
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
 {
+    if (g.op_a != 0 || g.op_b != 0) return cudaErrorInvalidValue;   // transposed operands arrive packed
     switch (kernel) {
     case kKernFfma128x128k32s4: return launch<CfgFfma128x128k32s4>(g, stream);
     case kKernFfma2_128x128k32s4: return launch<CfgFfma2_128x128k32s4>(g, stream);

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_constant__ CUtensorMap mapAlo,
                     const __grid_constant__ CUtensorMap mapBhi, const __grid_constant__ CUtensorMap mapBlo,
                     float *__restrict__ C, int64_t ldc, int M, int N, const Schedule sched,
-                    unsigned int *status)
+                    unsigned int *status, float alpha, float beta)
 {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -263,14 +263,26 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                 }
                 if (row < M) {
                     const int col0 = col_base + c0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] *= alpha;
                     if (VEC_C && col0 + 32 <= N) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+                            float4 v = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                            if (beta != 0.0f) {
+                                const float4 o = *p;
+                                v.x = fmaf(beta, o.x, v.x);
+                                v.y = fmaf(beta, o.y, v.y);
+                                v.z = fmaf(beta, o.z, v.z);
+                                v.w = fmaf(beta, o.w, v.w);
+                            }
+                            *p = v;
+                        }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = f[j];
+                            if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], f[j]) : f[j];
                     }
                 }
             }
@@ -376,6 +388,25 @@ cudaError_t encode_kmajor(CUtensorMap *map, const float *ptr, int64_t rows, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// K-major hi/lo split of an operand with `rows` rows of K values: stored
+// K-major (rows x K, leading dimension ld) when `kmajor`, else transposed
+// (K x rows, leading dimension ld).
+cudaError_t split_kmajor(const float *src, bool kmajor, int64_t rows, int64_t K, int64_t ld, float *hi,
+                         float *lo, int64_t kp, int num_sms, cudaStream_t stream)
+{
+    if (kmajor) {
+        const int64_t gy = rows < 65535 ? rows : 65535;
+        int64_t gx = (K + 255) / 256;
+        if (gx > 64) gx = 64;
+        tf32_split_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(src, rows, K, ld, hi, lo, kp);
+    } else {
+        const int64_t tiles = ((K + 31) / 32) * ((rows + 31) / 32);
+        const unsigned grid = (unsigned)(tiles < (int64_t)num_sms * 32 ? tiles : (int64_t)num_sms * 32);
+        tf32_split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(src, K, rows, ld, hi, lo, kp);
+    }
+    return cudaGetLastError();
+}
+
 using Tf32x3Wide = Tf32x3Cfg<256, 4>;    // 128 x 256 tiles, 4 stages of 48 KB
 using Tf32x3Square = Tf32x3Cfg<128, 6>;  // 128 x 128 tiles, 6 stages of 32 KB
 
@@ -413,19 +444,13 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     float *b_lo = reinterpret_cast<float *>(ws + 2 * l.a_bytes + l.b_bytes);
     cudaError_t e;
 
-    // Split pre-passes: A row by row; B transposed to K-major.
-    {
-        const int64_t gy = g.M < 65535 ? g.M : 65535;
-        int64_t gx = (g.K + 255) / 256;
-        if (gx > 64) gx = 64;
-        tf32_split_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(g.A, g.M, g.K, g.lda, a_hi,
-                                                                                   a_lo, l.kp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const int64_t tiles = ((g.K + 31) / 32) * ((g.N + 31) / 32);
-        const unsigned grid = (unsigned)(tiles < (int64_t)g.num_sms * 32 ? tiles : (int64_t)g.num_sms * 32);
-        tf32_split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(g.B, g.K, g.N, g.ldb, b_hi, b_lo, l.kp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    // Split pre-passes into K-major hi/lo copies: a K-major operand (A as
+    // stored, or B stored transposed) is split row by row, the others go
+    // through the transposing split.
+    if ((e = split_kmajor(g.A, g.op_a == 0, g.M, g.K, g.lda, a_hi, a_lo, l.kp, g.num_sms, stream)) != cudaSuccess)
+        return e;
+    if ((e = split_kmajor(g.B, g.op_b == 1, g.N, g.K, g.ldb, b_hi, b_lo, l.kp, g.num_sms, stream)) != cudaSuccess)
+        return e;
 
     CUtensorMap mAh, mAl, mBh, mBl;
     if ((e = encode_kmajor(&mAh, a_hi, g.M, g.K, l.kp, Cfg::BM, Cfg::BK)) != cudaSuccess) return e;
@@ -444,7 +469,8 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     int64_t ldc = g.ldc;
     int M = (int)g.M, N = (int)g.N;
     unsigned int *status = g.status;
-    void *args[] = {&mAh, &mAl, &mBh, &mBl, &C, &ldc, &M, &N, &sched, &status};
+    float alpha = g.alpha, beta = g.beta;
+    void *args[] = {&mAh, &mAl, &mBh, &mBl, &C, &ldc, &M, &N, &sched, &status, &alpha, &beta};
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, false>);
     // Owners wait on other CTAs' partial sums: all CTAs must be resident.
@@ -471,7 +497,18 @@ cudaError_t prepare_tf32x3()
 
 cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream)
 {
-    return kernel == kKernTf32x3_128x128 ? launch_cfg<Tf32x3Square>(g, stream) : launch_cfg<Tf32x3Wide>(g, stream);
+    // Batch entries run one after another, reusing the split buffers.
+    for (int64_t b = 0; b < (g.batch > 1 ? g.batch : 1); ++b) {
+        GemmArgs e = g;
+        e.A = g.A + b * g.stride_a;
+        e.B = g.B + b * g.stride_b;
+        e.C = g.C + b * g.stride_c;
+        e.batch = 1;
+        const cudaError_t r = kernel == kKernTf32x3_128x128 ? launch_cfg<Tf32x3Square>(e, stream)
+                                                            : launch_cfg<Tf32x3Wide>(e, stream);
+        if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace sgemm_gb300

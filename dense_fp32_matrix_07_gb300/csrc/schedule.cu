@@ -12,13 +12,14 @@ size_t flag_bytes(const Schedule &s, int flags_per_cta)
 }  // namespace
 
 Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
-                       bool with_sk)
+                       bool with_sk, int64_t batch)
 {
     Schedule s{};
     s.tiles_m = (int)((M + bm - 1) / bm);
     s.tiles_n = (int)((N + bn - 1) / bn);
     s.nk = (int)((K + bk - 1) / bk);
-    s.tiles = (int64_t)s.tiles_m * s.tiles_n;
+    s.tiles_per_batch = (int64_t)s.tiles_m * s.tiles_n;
+    s.tiles = s.tiles_per_batch * (batch > 0 ? batch : 1);
     s.dp_tiles = s.tiles;
     s.sk_iters = 0;
     s.sk_ctas = 0;

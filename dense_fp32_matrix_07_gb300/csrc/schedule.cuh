@@ -43,9 +43,10 @@ __device__ __forceinline__ bool wait_flag(const unsigned *flag)
 // thread of the kernel.
 struct Schedule {
     int tiles_m, tiles_n;
+    int64_t tiles_per_batch;   // tiles_m * tiles_n
     int nk;             // K slabs per tile
     int grid;           // CTAs launched
-    int64_t tiles;      // all output tiles
+    int64_t tiles;      // all output tiles, batch entry after batch entry
     int64_t dp_tiles;   // whole-tile work: tiles [0, dp_tiles), round-robin
     int64_t sk_iters;   // slab iterations of the stream-K region
     int sk_ctas;        // CTAs [0, sk_ctas) share those iterations
@@ -117,6 +118,15 @@ __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n,
     tn = (int)(local / rows);
 }
 
+// Batch entry and tile of linear tile index t (batch entries one after the
+// other, the grouped order within each).
+__device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_t t, int &b, int &tm, int &tn)
+{
+    const int64_t bb = t / s.tiles_per_batch;
+    b = (int)bb;
+    tile_coords(t - bb * s.tiles_per_batch, s.tiles_m, s.tiles_n, tm, tn);
+}
+
 // ------------------------------- host side -------------------------------
 
 // Plans the schedule of an M x N x K product in bm x bn tiles with bk-deep
@@ -128,7 +138,7 @@ __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n,
 // tile cut into floor(slots / leftover) >= 2 equal K parts. `with_sk` false
 // always gives whole tiles. Pointers are left null.
 Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
-                       bool with_sk);
+                       bool with_sk, int64_t batch = 1);
 
 // Workspace bytes of a stream-K schedule: flags (`flags_per_cta` per CTA,
 // rounded to 256 bytes) then one bm x bn FP32 partial-sum slot per CTA.

@@ -176,50 +176,112 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_
 
 namespace sgemm_gb300 {
 
-// sgemm_ex() with two test-only knobs: a forced schedule policy (-1: the
-// configuration's own) and a copy for CTA 0's producer to withhold (-1: none).
-static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
-                      const float *B, int64_t ldb, float *C, int64_t ldc, int config,
-                      int sched_override, int withhold_it, cudaStream_t stream)
-{
-    if (config < -1 || config >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
-    int rc = check_sizes(M, N, K, lda, ldb, ldc);
-    if (rc != SGEMM_OK) return rc;
-    if (M == 0 || N == 0) return SGEMM_OK;
-    if (C == nullptr) return SGEMM_ERR_INVALID_VALUE;
-    if (K > 0 && (A == nullptr || B == nullptr)) return SGEMM_ERR_INVALID_VALUE;
+// One call of the general form alpha * op(A_b) . op(B_b) + beta * C_b.
+struct Call {
+    int op_a, op_b;
+    int64_t M, N, K;
+    float alpha;
+    const float *A;
+    int64_t lda, sa;
+    const float *B;
+    int64_t ldb, sb;
+    float beta;
+    float *C;
+    int64_t ldc, sc;
+    int64_t batch;
+    int config;          // -1: automatic
+    int sched_override;  // -1: the configuration's policy (test knob)
+    int withhold_it;     // -1: none (test knob)
+};
 
-    const uint64_t a = (uint64_t)(uintptr_t)A, b = (uint64_t)(uintptr_t)B,
-                   c = (uint64_t)(uintptr_t)C;
-    const int64_t c_elems = extent(M, N, ldc);
-    if (K > 0 && (overlaps(c, c_elems, a, extent(M, K, lda)) ||
-                  overlaps(c, c_elems, b, extent(K, N, ldb))))
-        return SGEMM_ERR_INVALID_VALUE;
+// Elements spanned by `batch` entries of extent `e` at stride `s`, or -1.
+static int64_t batch_extent(int64_t e, int64_t s, int64_t batch)
+{
+    if (e <= 0) return e;
+    const __int128 t = (__int128)(batch - 1) * s + e;
+    if (t * 4 > (__int128)INT64_MAX) return -1;
+    return (int64_t)t;
+}
+
+static int sgemm_call(const Call &c, cudaStream_t stream)
+{
+    if (c.config < -1 || c.config >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
+    if ((c.op_a != 0 && c.op_a != 1) || (c.op_b != 0 && c.op_b != 1)) return SGEMM_ERR_INVALID_VALUE;
+    if (c.M < 0 || c.N < 0 || c.K < 0 || c.batch < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (c.sa < 0 || c.sb < 0 || c.sc < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (c.batch == 0 || c.M == 0 || c.N == 0) return SGEMM_OK;
+    // Stored shapes: A is M x K (op 0) or K x M (op 1); B is K x N or N x K.
+    const int64_t a_rows = c.op_a ? c.K : c.M, a_cols = c.op_a ? c.M : c.K;
+    const int64_t b_rows = c.op_b ? c.N : c.K, b_cols = c.op_b ? c.K : c.N;
+    const bool reads_ab = c.K > 0 && c.alpha != 0.0f;
+    if (c.ldc < c.N || c.ldc < 1) return SGEMM_ERR_INVALID_VALUE;
+    if (reads_ab && (c.lda < a_cols || c.ldb < b_cols || c.lda < 1 || c.ldb < 1)) return SGEMM_ERR_INVALID_VALUE;
+    if (c.M > kMaxDim || c.N > kMaxDim || c.K > kMaxDim) return SGEMM_ERR_OVERFLOW;
+    const int64_t c_one = extent(c.M, c.N, c.ldc);
+    if (c_one < 0) return SGEMM_ERR_OVERFLOW;
+    if (c.batch > 1 && c.sc < c_one) return SGEMM_ERR_INVALID_VALUE;   // C entries must not overlap
+    const int64_t c_all = batch_extent(c_one, c.sc, c.batch);
+    if (c_all < 0) return SGEMM_ERR_OVERFLOW;
+    if (c.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    const uint64_t a = (uint64_t)(uintptr_t)c.A, b = (uint64_t)(uintptr_t)c.B, cp = (uint64_t)(uintptr_t)c.C;
+    int64_t a_all = 0, b_all = 0;
+    if (reads_ab) {
+        if (c.A == nullptr || c.B == nullptr) return SGEMM_ERR_INVALID_VALUE;
+        const int64_t a_one = extent(a_rows, a_cols, c.lda), b_one = extent(b_rows, b_cols, c.ldb);
+        if (a_one < 0 || b_one < 0) return SGEMM_ERR_OVERFLOW;
+        a_all = batch_extent(a_one, c.sa, c.batch);
+        b_all = batch_extent(b_one, c.sb, c.batch);
+        if (a_all < 0 || b_all < 0) return SGEMM_ERR_OVERFLOW;
+        if (overlaps(cp, c_all, a, a_all) || overlaps(cp, c_all, b, b_all)) return SGEMM_ERR_INVALID_VALUE;
+    }
+    const bool plain = c.op_a == 0 && c.op_b == 0 && c.alpha == 1.0f && c.beta == 0.0f && c.batch == 1;
 
     DeviceState *dev = nullptr;
-    rc = device_state(&dev);
+    int rc = device_state(&dev);
     if (rc != SGEMM_OK) return rc;
 
-    if (K == 0) {
-        if (launch_zero_fill(C, M, N, ldc, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-        return SGEMM_OK;
+    if (!reads_ab) {
+        // The empty sum (K == 0) or alpha == 0: C = beta * C.
+        if (c.beta == 1.0f) return SGEMM_OK;
+        return launch_scale(c.C, c.M, c.N, c.ldc, c.sc, c.batch, c.beta, stream) == cudaSuccess
+                   ? SGEMM_OK
+                   : SGEMM_ERR_LAUNCH;
     }
 
-    const ProblemShape p{M, N, K, lda, ldb, ldc, a, b, c, dev->num_sms};
-    const int cfg = config < 0 ? select_config(p) : config;
+    const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, dev->num_sms};
+    const int cfg = c.config < 0 ? select_config(p) : c.config;
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
+    // Kernels without TMA (the simple and ladder kernels) run the plain form only.
+    if (!plain && !kConfigTable[cfg].uses_tma) return SGEMM_ERR_UNSUPPORTED;
 
-    GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
-    g.sched = sched_override >= 0 ? sched_override : kConfigTable[cfg].sched;
-    g.withhold_it = withhold_it;
-    // One scratch allocation, carved into: packed A, packed B (rows padded to
-    // a multiple of 32 floats = 128 bytes), then the stream-K workspace.
+    GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
+    g.sched = c.sched_override >= 0 ? c.sched_override : kConfigTable[cfg].sched;
+    g.withhold_it = c.withhold_it;
+    g.alpha = c.alpha;
+    g.beta = c.beta;
+    g.batch = c.batch;
+    g.stride_a = c.batch > 1 ? c.sa : 0;
+    g.stride_b = c.batch > 1 ? c.sb : 0;
+    g.stride_c = c.batch > 1 ? c.sc : 0;
+    g.op_a = c.op_a;
+    g.op_b = c.op_b;
+
+    // TMA FFMA configurations read A (M x K) and B (K x N) in place when the
+    // rows and batch strides are 16-byte multiples on a 16-byte-aligned base;
+    // anything else (a transposed operand included) is packed into scratch,
+    // rows padded to 32 floats. A shared operand (batch stride 0) is packed once.
     const bool packs = kConfigTable[cfg].packs;
-    const bool pa = packs && needs_pack(a, lda), pb = packs && needs_pack(b, ldb);
-    const int64_t lda_p = round_up(K, 32), ldb_p = round_up(N, 32);
-    const size_t a_bytes = pa ? (size_t)(M * lda_p) * 4 : 0;
-    const size_t b_bytes = pb ? (size_t)(K * ldb_p) * 4 : 0;
+    auto stride_ok = [&](int64_t s, int64_t one) { return c.batch <= 1 || s == 0 || (s % 4 == 0 && s >= one); };
+    const bool pa = packs && (c.op_a == 1 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.M * c.lda));
+    const bool pb = packs && (c.op_b == 1 || needs_pack(b, c.ldb) || !stride_ok(c.sb, c.K * c.ldb));
+    const int64_t lda_p = round_up(c.K, 32), ldb_p = round_up(c.N, 32);
+    const int64_t a_entries = (c.batch > 1 && c.sa != 0) ? c.batch : 1;
+    const int64_t b_entries = (c.batch > 1 && c.sb != 0) ? c.batch : 1;
+    const size_t a_bytes = pa ? (size_t)(a_entries * c.M * lda_p) * 4 : 0;
+    const size_t b_bytes = pb ? (size_t)(b_entries * c.K * ldb_p) * 4 : 0;
     const size_t ws_off = (a_bytes + b_bytes + 255) / 256 * 256;
+    if (pa) g.op_a = 0;
+    if (pb) g.op_b = 0;
     const size_t ws_bytes = config_workspace_bytes(cfg, g);
     const size_t total = ws_off + ws_bytes;
     uint8_t *scratch = nullptr;
@@ -228,23 +290,31 @@ static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
             cudaGetLastError();
             return SGEMM_ERR_ALLOC;
         }
+        cudaError_t e = cudaSuccess;
         if (pa) {
             float *dst = reinterpret_cast<float *>(scratch);
-            if (launch_pack(A, M, K, lda, dst, lda_p, stream) != cudaSuccess) {
-                cudaFreeAsync(scratch, stream);
-                return SGEMM_ERR_LAUNCH;
-            }
+            e = c.op_a == 1 ? launch_pack_transpose_batched(c.A, c.K, c.M, c.lda, c.sa, dst, lda_p, c.M * lda_p,
+                                                            a_entries, stream)
+                            : launch_pack_batched(c.A, c.M, c.K, c.lda, c.sa, dst, lda_p, c.M * lda_p, a_entries,
+                                                  stream);
             g.A = dst;
             g.lda = lda_p;
+            g.stride_a = a_entries > 1 ? c.M * lda_p : 0;
         }
-        if (pb) {
+        if (e == cudaSuccess && pb) {
             float *dst = reinterpret_cast<float *>(scratch + a_bytes);
-            if (launch_pack(B, K, N, ldb, dst, ldb_p, stream) != cudaSuccess) {
-                cudaFreeAsync(scratch, stream);
-                return SGEMM_ERR_LAUNCH;
-            }
+            e = c.op_b == 1 ? launch_pack_transpose_batched(c.B, c.N, c.K, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p,
+                                                            b_entries, stream)
+                            : launch_pack_batched(c.B, c.K, c.N, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p, b_entries,
+                                                  stream);
             g.B = dst;
             g.ldb = ldb_p;
+            g.stride_b = b_entries > 1 ? c.K * ldb_p : 0;
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaFreeAsync(scratch, stream);
+            return SGEMM_ERR_LAUNCH;
         }
         if (ws_bytes > 0) {
             g.workspace = scratch + ws_off;
@@ -259,6 +329,14 @@ static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
         return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
+}
+
+static int sgemm_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float *C, int64_t ldc, int config, int sched_override, int withhold_it, cudaStream_t stream)
+{
+    const Call c{0, 0, M, N, K, 1.0f, A, lda, 0, B, ldb, 0, 0.0f, C, ldc, 0, 1,
+                 config, sched_override, withhold_it};
+    return sgemm_call(c, stream);
 }
 
 }  // namespace sgemm_gb300
@@ -285,6 +363,23 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K, const float *A, in
     // Whole tiles: no stream-K waits between CTAs, only the withheld copy.
     return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, kSchedDataParallel,
                       slab < 0 ? -1 : slab, stream);
+}
+
+int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                     int64_t lda, int64_t stride_a, const float *B, int64_t ldb, int64_t stride_b, float beta,
+                     float *C, int64_t ldc, int64_t stride_c, int64_t batch, int config, cudaStream_t stream)
+{
+    const Call c{op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc, stride_c, batch,
+                 config, -1, -1};
+    return sgemm_call(c, stream);
+}
+
+int sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                  int64_t stride_a, const float *B, int64_t ldb, int64_t stride_b, float beta, float *C,
+                  int64_t ldc, int64_t stride_c, int64_t batch, cudaStream_t stream)
+{
+    return sgemm_general_ex(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
+                            stride_c, batch, -1, stream);
 }
 
 int sgemm_check_status(cudaStream_t stream)

@@ -112,6 +112,49 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K,
              int config, cudaStream_t stream);
 
 /*
+ * sgemm_general — the BLAS-style general form, over a strided batch:
+ *
+ *     C_b = alpha * op(A_b) . op(B_b) + beta * C_b      for 0 <= b < batch
+ *
+ * An extension for users of this library; the pages define only C = A . B
+ * (the definition at the top of this file, which this reduces to with
+ * op_a = op_b = 0, alpha = 1, beta = 0, batch = 1).
+ *
+ *   op_a      0: A_b is stored M x K (row i at A + b*stride_a + i*lda,
+ *             lda >= K); 1: A_b is stored transposed, K x M (lda >= M).
+ *   op_b      0: B_b stored K x N (ldb >= N); 1: stored N x K (ldb >= K).
+ *   alpha     scales the product. alpha == 0 (or K == 0) reads neither A
+ *             nor B: C_b = beta * C_b.
+ *   beta      scales the old C. beta == 0: C is written without being read
+ *             (it may hold NaN); beta == 1 with alpha == 0 is a no-op.
+ *   stride_a, stride_b, stride_c
+ *             batch strides in elements (>= 0; ignored when batch == 1). A
+ *             stride of 0 shares one A (or B) across the batch; C entries
+ *             must not overlap (stride_c >= (M-1)*ldc + N when batch > 1).
+ *   batch     number of products (0 is a no-op).
+ *
+ * Pointers are device pointers; C must not overlap A or B (over the whole
+ * batch). Transposed operands and rows or batch strides that are not 16-byte
+ * multiples are packed into pool scratch first; alpha and beta are applied in
+ * the kernels' epilogues; batch entries share one persistent launch (their
+ * tiles are one schedule). Status codes as sgemm(); SGEMM_ERR_UNSUPPORTED if
+ * a forced configuration cannot run the general form (the simple and the
+ * kernel-ladder configurations run only the plain form).
+ */
+int sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                  const float *A, int64_t lda, int64_t stride_a,
+                  const float *B, int64_t ldb, int64_t stride_b,
+                  float beta, float *C, int64_t ldc, int64_t stride_c,
+                  int64_t batch, cudaStream_t stream);
+
+/* sgemm_general() with a forced kernel configuration (-1 = automatic). */
+int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, int64_t stride_a,
+                     const float *B, int64_t ldb, int64_t stride_b,
+                     float beta, float *C, int64_t ldc, int64_t stride_c,
+                     int64_t batch, int config, cudaStream_t stream);
+
+/*
  * sgemm_check_status — waits for `stream`, then reads and clears the current
  * device's error word. Returns SGEMM_ERR_TIMEOUT if any kernel of this
  * library on the device gave up a bounded wait since the last check (its
