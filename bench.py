@@ -19,8 +19,13 @@ Also reported on the same JSON line:
                 stream) against the FFMA peak SMs x 128 lanes x 2 FLOP x max
                 SM clock ("alu"-bound: the intensity is far above the HBM
                 ridge), with DRAM traffic from the committed ncu summary;
-  cpu_baseline  the FP64 CPU oracle timed on this host's cores over a bounded
-                sample of C's rows;
+  cpu_baseline  the FP64 CPU oracle timed on this host's cores: the whole
+                product when it takes under ~30 s, else the sampled rows and
+                columns the parity tests check, else a bounded row sample
+                (--cpu-threads 1 gives the single-core figure);
+  step_ms       median, best and mean device time of the timed steps;
+  warm          for workloads that fit in L2 (timed with an L2 flush before
+                every step), the same steps back to back without the flush;
   clocks        nvidia-smi samples taken during the timed region.
 --impl reference times that oracle alone as the reference arm.
 """
@@ -297,24 +302,55 @@ def workload_config(w, kernel, l2=None):
             "ldc": w.ldc, "dist": w.dist, "seed": w.seed, "kernel": kernel, "l2": l2}
 
 
-def cpu_baseline(w, A, B):
-    """The oracle on this host's cores over a bounded sample (~10 s) of rows."""
+def cpu_baseline(w, A, B, threads=0, budget_s=30.0, min_s=10.0):
+    """The oracle on this host's cores. The unit of work is the whole
+    product when that fits in about `budget_s` seconds; otherwise the rows
+    and columns of C that the parity tests check on a sampled workload;
+    otherwise a bounded sample of full rows. The unit is repeated until at
+    least `min_s` seconds have been timed. `threads` > 0 pins the oracle's
+    thread count."""
     import numpy as np
     import oracle
     oracle.build()
+    if threads > 0:
+        oracle.set_num_threads(threads)
     An, Bn = A.numpy(), B.numpy()
     probe = np.arange(min(w.M, oracle.num_threads()), dtype=np.int64)
     t0 = time.perf_counter()
     oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, probe, want_abs=False)
     per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
-    nrows = int(max(oracle.num_threads(), min(w.M, 10.0 / per_row)))
-    rows = workloads.sample_indices(w.M, nrows, 77)
+    if per_row * w.M <= budget_s:
+        def unit():
+            oracle.sgemm(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, want_abs=False)
+        done = product_flops(w.M, w.N, w.K)
+        what = f"the whole product ({w.M}x{w.N}x{w.K})"
+    elif w.sampled and per_row * (256 * (1 + w.N / w.M)) <= budget_s:
+        rows = workloads.sample_indices(w.M, 256, w.seed + 1000)
+        cols = workloads.sample_indices(w.N, 256, w.seed + 2000)
+
+        def unit():
+            oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, rows, want_abs=False)
+            oracle.sgemm_cols(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, cols, want_abs=False)
+        done = product_flops(len(rows), w.N, w.K) + product_flops(w.M, len(cols), w.K)
+        what = (f"the {len(rows)} rows and {len(cols)} columns of C the parity test checks "
+                f"({len(rows)}x{w.N}x{w.K} + {w.M}x{len(cols)}x{w.K})")
+    else:
+        nrows = int(max(oracle.num_threads(), min(w.M, (budget_s / 3) / per_row)))
+        rows = workloads.sample_indices(w.M, nrows, 77)
+
+        def unit():
+            oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, rows, want_abs=False)
+        done = product_flops(len(rows), w.N, w.K)
+        what = f"{len(rows)} sampled full rows of C ({len(rows)}x{w.N}x{w.K})"
+    reps, dt = 0, 0.0
     t0 = time.perf_counter()
-    oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb, rows, want_abs=False)
-    dt = time.perf_counter() - t0
-    return {"value": round(job_gflops(product_flops(len(rows), w.N, w.K), 1, 1, dt), 3), "unit": "GFLOP/s",
+    while dt < min_s or reps == 0:
+        unit()
+        reps += 1
+        dt = time.perf_counter() - t0
+    return {"value": round(job_gflops(done, reps, 1, dt), 3), "unit": "GFLOP/s",
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} sampled full rows of C ({len(rows)}x{w.N}x{w.K}), {dt:.1f} s"}
+            "sample": f"{what} x {reps}, {dt:.1f} s"}
 
 
 def main():
@@ -330,6 +366,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs (config sweeps)")
     ap.add_argument("--no-tf32x3", action="store_true",
                     help="skip the separately reported 3xTF32 tensor-core measurement")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="oracle threads for cpu_baseline (default: all host cores)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -414,6 +452,25 @@ def main():
 
     (t_max,) = max_over_ranks([step_s], pg, dev)
     value = job_gflops(flops, args.steps, world, t_max)
+
+    # An L2-resident workload is also timed warm: the same steps back to
+    # back, operands left in L2 by the previous step.
+    warm = None
+    if flush is not None:
+        warm_steps = min(args.steps, 200)
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(warm_steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if sg.sgemm_check_status(sh) != 0:
+            raise RuntimeError("device status after the warm steps")
+        (warm_s,) = max_over_ranks([ev0.elapsed_time(ev1) / 1e3], pg, dev)
+        warm = {"value": round(job_gflops(flops, warm_steps, world, warm_s), 1), "unit": "GFLOP/s",
+                "steps": warm_steps, "ms_per_step": round(warm_s / warm_steps * 1e3, 4),
+                "note": "back-to-back steps, no L2 flush between them"}
 
     # ---- e2e: host buffers, copies inside the timing ----
     # Every step copies A and B in from pinned host memory, runs the product
@@ -565,6 +622,9 @@ def main():
                 "steps": e2e_steps,
                 "mode": "pipelined: 2 buffer sets, H2D / product / D2H on 3 streams",
                 "serial_value": round(serial_value, 1)},
+        "step_ms": {"median": round(statistics.median(kernel_ms), 4), "best": round(min(kernel_ms), 4),
+                    "mean": round(statistics.mean(kernel_ms), 4)},
+        "warm": warm,
         "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": "alu", "achieved": round(achieved_tflops, 3),
                      "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
@@ -580,7 +640,7 @@ def main():
         line["roofline"]["frac_at_sampled_clock"] = round(
             achieved_tflops / (peak_tflops * clocks["sm_mhz"] / sm_max), 4)
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, A, B)
+        line["cpu_baseline"] = cpu_baseline(w, A, B, args.cpu_threads)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
