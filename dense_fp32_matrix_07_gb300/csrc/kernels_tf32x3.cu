@@ -304,16 +304,35 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
 }
 
 // hi[i * ldo + k] = tf32(x), lo[i * ldo + k] = tf32(x - hi) for x = src[i * ld + k].
-__global__ void tf32_split_rows_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t ld,
-                                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldo)
+// One block per row at a time; VEC reads and writes float4 (source rows and
+// base 16-byte aligned, cols a multiple of 4), otherwise single floats.
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+tf32_split_rows_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t ld,
+                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldo)
 {
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
-             c += (int64_t)gridDim.x * blockDim.x) {
-            const float x = src[r * ld + c];
-            const float h = ptx::to_tf32(x);
-            hi[r * ldo + c] = h;
-            lo[r * ldo + c] = ptx::to_tf32(x - h);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *s = src + r * ld;
+        float *h = hi + r * ldo;
+        float *l = lo + r * ldo;
+        if (VEC) {
+            for (int64_t c = threadIdx.x; c < cols / 4; c += blockDim.x) {
+                const float4 x = reinterpret_cast<const float4 *>(s)[c];
+                float4 xh, xl;
+                xh.x = ptx::to_tf32(x.x); xl.x = ptx::to_tf32(x.x - xh.x);
+                xh.y = ptx::to_tf32(x.y); xl.y = ptx::to_tf32(x.y - xh.y);
+                xh.z = ptx::to_tf32(x.z); xl.z = ptx::to_tf32(x.z - xh.z);
+                xh.w = ptx::to_tf32(x.w); xl.w = ptx::to_tf32(x.w - xh.w);
+                reinterpret_cast<float4 *>(h)[c] = xh;
+                reinterpret_cast<float4 *>(l)[c] = xl;
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+                const float x = s[c];
+                const float xh = ptx::to_tf32(x);
+                h[c] = xh;
+                l[c] = ptx::to_tf32(x - xh);
+            }
         }
     }
 }
@@ -395,10 +414,15 @@ cudaError_t split_kmajor(const float *src, bool kmajor, int64_t rows, int64_t K,
                          float *lo, int64_t kp, int num_sms, cudaStream_t stream)
 {
     if (kmajor) {
-        const int64_t gy = rows < 65535 ? rows : 65535;
-        int64_t gx = (K + 255) / 256;
-        if (gx > 64) gx = 64;
-        tf32_split_rows_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(src, rows, K, ld, hi, lo, kp);
+        // kp is a multiple of 4 and the planes are 256-byte aligned, so the
+        // writes vectorise whenever the source rows do.
+        const bool vec = K % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+        const int64_t cap = (int64_t)num_sms * 8;
+        const unsigned grid = (unsigned)(rows < cap ? rows : cap);
+        if (vec)
+            tf32_split_rows_kernel<true><<<grid, 256, 0, stream>>>(src, rows, K, ld, hi, lo, kp);
+        else
+            tf32_split_rows_kernel<false><<<grid, 256, 0, stream>>>(src, rows, K, ld, hi, lo, kp);
     } else {
         const int64_t tiles = ((K + 31) / 32) * ((rows + 31) / 32);
         const unsigned grid = (unsigned)(tiles < (int64_t)num_sms * 32 ? tiles : (int64_t)num_sms * 32);
