@@ -43,7 +43,8 @@ struct GemmArgs {
 
 // Bits of the device error word.
 enum : unsigned int {
-    kStatusTimeout = 1u,   // a bounded wait gave up
+    kStatusTimeout = 1u,        // a bounded wait gave up
+    kStatusLaunchConfig = 2u,   // a kernel found its launch shape wrong and did nothing
 };
 
 // Probe-count backstop of the device-side waits. Their primary bound is wall

@@ -23,6 +23,8 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"tf32x3_128x256_k16_s4_auto", kKernTf32x3_128x256, kSchedAuto, true, false, 128, 256},
     {"tf32x3_128x128_k16_s6", kKernTf32x3_128x128, kSchedDataParallel, true, false, 128, 128},
     {"tf32x3_128x256_k16_s4_dp", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
+    {"tf32x3_pair_128x256_k16_s4", kKernTf32x3_pair, kSchedTailSplit, true, false, 128, 256},
+    {"tf32x3_pair_128x256_k16_s4_dp", kKernTf32x3_pair, kSchedDataParallel, true, false, 128, 256},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)

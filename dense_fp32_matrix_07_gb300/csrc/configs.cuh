@@ -31,7 +31,8 @@ enum KernelId : int {
     kKernLadderRegisterTiled2x2, // 16x16 padded smem tiles, 2x2 per thread
     // Tensor cores (kernels_tf32x3.cu): 3xTF32 split, tcgen05.mma into TMEM.
     kKernTf32x3_128x256,
-    kKernTf32x3_128x128
+    kKernTf32x3_128x128,
+    kKernTf32x3_pair            // 128x256 per CTA, clusters of 2 along M multicasting B
 };
 
 // Configurations = kernel instance + schedule policy.
@@ -55,6 +56,8 @@ enum ConfigId : int {
     kCfgTf32x3_128x256_auto,
     kCfgTf32x3_128x128,
     kCfgTf32x3_128x256_dp,
+    kCfgTf32x3_pair,
+    kCfgTf32x3_pair_dp,
     kNumConfigs
 };
 

@@ -31,8 +31,18 @@
 // The accumulator is double-buffered (2 x 256 of the 512 TMEM columns), so
 // the epilogue of one tile overlaps the MMAs of the next. Every wait is
 // bounded in time; a role that gives up sets the device error word and skips
-// to the teardown (a named barrier of the MMA and epilogue warps, then TMEM
-// is freed); the producer drains its own copies before leaving.
+// to the teardown (a CTA-wide barrier, then TMEM is freed); the producer
+// drains its own copies before leaving.
+//
+// Cluster-pair variant (CM = 2): two CTAs of a cluster compute vertically
+// adjacent 128 x 256 tiles that share one B tile. Each loads half of B_hi and
+// B_lo and multicasts it into both CTAs' stage, so a CTA moves 32 KB per slab
+// instead of 48 KB; each MMA warp multicasts its stage-release commit to both
+// CTAs' empty barriers (count 2), so no stage is refilled before both have
+// consumed it. Before leaving, a CTA's producer waits for the last release
+// of every stage from both CTAs (no peer commit can then still be on its
+// way), and the CTAs exchange a bounded "done" handshake. A launch without
+// the cluster is detected (cluster size != 2) and reported, not run.
 #include "common.cuh"
 #include "configs.cuh"
 #include "ptx.cuh"
@@ -45,14 +55,16 @@ namespace sgemm_gb300 {
 
 namespace {
 
-template <int BN_, int STAGES_>
+template <int BN_, int STAGES_, int CM_ = 1>
 struct Tf32x3Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 16, STAGES = STAGES_;
+    static constexpr int CM = CM_;                             // CTAs per cluster, along M
     static constexpr int ROW_BYTES = BK * 4;                   // 64: 64-byte swizzle
     static constexpr int A_TILE = BM * ROW_BYTES;              // 8 KB
     static constexpr int B_TILE = BN * ROW_BYTES;              // 16 KB
+    static constexpr int B_PIECE_ROWS = BN / CM;               // rows of B each CTA of a cluster loads
     static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;    // full, empty, acc full, acc empty, drain
+    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1 + 1;  // full, empty, acc full, acc empty, drain, exit
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_COLS = 2 * BN;                   // double-buffered FP32 accumulator
     static constexpr int THREADS = 256;
@@ -60,6 +72,8 @@ struct Tf32x3Cfg {
     static constexpr uint32_t IDESC = ptx::idesc_tf32_kmajor(BM, BN);
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(TMEM_COLS <= 512, "tensor memory columns");
+    static_assert(CM == 1 || CM == 2 || CM == 4, "cluster size");
+    static_assert((B_PIECE_ROWS * ROW_BYTES) % 1024 == 0, "B pieces keep the swizzle phase");
 };
 
 template <class Cfg, bool VEC_C>
@@ -69,7 +83,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                     float *__restrict__ C, int64_t ldc, int M, int N, const Schedule sched,
                     unsigned int *status, float alpha, float beta)
 {
-    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES, CM = Cfg::CM;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -83,73 +97,117 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
     auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    const uint32_t exit_bar = bars + 8u * (2 * STAGES + 5);
     const uint32_t tmem_slot = bars + 8u * Cfg::NUM_BARS;
     uint32_t *tmem_slot_ptr = reinterpret_cast<uint32_t *>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x;
+    // A cluster of CM CTAs shares one schedule item: CTA `rank` computes
+    // block row rank of the item's CM x 1 group of 128 x BN tiles.
+    const int rank = CM > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int g = (int)blockIdx.x / CM;               // schedule index (cluster)
+    const int slot = g * CM + rank;                   // this CTA's partial-sum slot and flags
     const int nk = sched.nk;
+    constexpr uint16_t kClusterMask = (uint16_t)((1u << CM) - 1u);
+    if constexpr (CM > 1) {
+        // Launched without its cluster of CM CTAs, this kernel would copy to
+        // and arrive at peers that do not exist: report it and do nothing.
+        if (ptx::cluster_nctarank() != (uint32_t)CM) {
+            if (threadIdx.x == 0) atomicOr(status, kStatusLaunchConfig);
+            return;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), CM);         // one MMA commit from every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
             ptx::mbar_init(acce_bar(b), 4);
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(exit_bar, CM);
         ptx::mbar_init_fence();
     }
     if (warp == 1) ptx::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     ptx::tc_fence_before();
-    __syncthreads();
+    // Barriers must be initialised in every CTA before any peer copies or
+    // arrives into them.
+    if constexpr (CM > 1)
+        ptx::cluster_sync_all();
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t taddr = *tmem_slot_ptr;
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane != 0) return;
-        ptx::prefetch_tensormap(&mapAhi);
-        ptx::prefetch_tensormap(&mapAlo);
-        ptx::prefetch_tensormap(&mapBhi);
-        ptx::prefetch_tensormap(&mapBlo);
-        const uint64_t policy = ptx::policy_evict_last();
-        int last_round[STAGES];
+        // A: this CTA's 128 rows. B: with CM > 1, this CTA loads rows
+        // [rank * BN/CM, (rank + 1) * BN/CM) of the B tile and multicasts
+        // them to the whole cluster, so each CTA's full barrier counts the
+        // whole stage; a stage is refilled only when every CTA's MMAs have
+        // released it (the empty barrier counts CM commits).
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&mapAhi);
+            ptx::prefetch_tensormap(&mapAlo);
+            ptx::prefetch_tensormap(&mapBhi);
+            ptx::prefetch_tensormap(&mapBlo);
+            const uint64_t policy = ptx::policy_evict_last();
+            int last_round[STAGES];
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
-        uint32_t it = 0;
-        bool ok = true;
-        Cursor cur = cursor_init(sched, g);
-        Item item;
-        while (ok && next_item(sched, cur, item)) {
-            int tm, tn;
-            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
-            for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
-                const int s = (int)(it % STAGES);
-                const int round = (int)(it / STAGES);
-                if (!ptx::wait_phase(empty_bar(s), (round & 1) ^ 1)) {
-                    atomicOr(status, kStatusTimeout);
-                    ok = false;
-                    break;
+            for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+            uint32_t it = 0;
+            bool ok = true;
+            Cursor cur = cursor_init(sched, g);
+            Item item;
+            while (ok && next_item(sched, cur, item)) {
+                int tg, tn;
+                tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tg, tn);
+                const int tm = tg * CM + rank;
+                for (int kb = item.kb0; kb < item.kb1; ++kb, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const int round = (int)(it / STAGES);
+                    if (!ptx::wait_phase(empty_bar(s), (round & 1) ^ 1)) {
+                        atomicOr(status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+                    ptx::tma_load_2d(stage_a_hi(s), &mapAhi, full_bar(s), kb * BK, tm * BM, policy);
+                    ptx::tma_load_2d(stage_a_lo(s), &mapAlo, full_bar(s), kb * BK, tm * BM, policy);
+                    if constexpr (CM > 1) {
+                        const uint32_t off = (uint32_t)(rank * Cfg::B_PIECE_ROWS * Cfg::ROW_BYTES);
+                        const int row = tn * BN + rank * Cfg::B_PIECE_ROWS;
+                        ptx::tma_load_2d_multicast(stage_b_hi(s) + off, &mapBhi, full_bar(s), kb * BK, row,
+                                                   kClusterMask, policy);
+                        ptx::tma_load_2d_multicast(stage_b_lo(s) + off, &mapBlo, full_bar(s), kb * BK, row,
+                                                   kClusterMask, policy);
+                    } else {
+                        ptx::tma_load_2d(stage_b_hi(s), &mapBhi, full_bar(s), kb * BK, tn * BN, policy);
+                        ptx::tma_load_2d(stage_b_lo(s), &mapBlo, full_bar(s), kb * BK, tn * BN, policy);
+                    }
+                    last_round[s] = round;
                 }
-                ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
-                ptx::tma_load_2d(stage_a_hi(s), &mapAhi, full_bar(s), kb * BK, tm * BM, policy);
-                ptx::tma_load_2d(stage_a_lo(s), &mapAlo, full_bar(s), kb * BK, tm * BM, policy);
-                ptx::tma_load_2d(stage_b_hi(s), &mapBhi, full_bar(s), kb * BK, tn * BN, policy);
-                ptx::tma_load_2d(stage_b_lo(s), &mapBlo, full_bar(s), kb * BK, tn * BN, policy);
-                last_round[s] = round;
+            }
+            // Every byte bound for this CTA (its own copies and the peers'
+            // multicasts) must have landed before it leaves.
+            for (int s = 0; s < STAGES; ++s)
+                if (last_round[s] >= 0 && !ptx::wait_phase(full_bar(s), last_round[s] & 1))
+                    atomicOr(status, kStatusTimeout);
+            // With CM > 1, so must every commit arrival the peers' MMA warps
+            // send to this CTA's empty barriers: wait for the release of each
+            // stage's last round by all CM CTAs (phase r of an empty barrier
+            // completes when round r of its stage has been released).
+            if constexpr (CM > 1) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (last_round[s] >= 0 && !ptx::wait_phase(empty_bar(s), last_round[s] & 1))
+                        atomicOr(status, kStatusTimeout);
             }
         }
-        for (int s = 0; s < STAGES; ++s)
-            if (last_round[s] >= 0 && !ptx::wait_phase(full_bar(s), last_round[s] & 1))
-                atomicOr(status, kStatusTimeout);
-        return;
-    }
-    if (warp == 2 || warp == 3) return;
-
-    if (warp == 1) {
+        __syncwarp();
+    } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             uint32_t it = 0, lt = 0;
@@ -183,17 +241,24 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                         ptx::mma_tf32(d, ah, bl, Cfg::IDESC, 1u);
                         ptx::mma_tf32(d, al, bh, Cfg::IDESC, 1u);
                     }
-                    ptx::mma_commit(empty_bar(s));   // the stage is free once these MMAs are done
+                    // The stage is free once these MMAs are done; with CM > 1
+                    // every CTA of the cluster learns it (their producers
+                    // multicast into this CTA's copy of the stage).
+                    if constexpr (CM > 1)
+                        ptx::mma_commit_multicast(empty_bar(s), kClusterMask);
+                    else
+                        ptx::mma_commit(empty_bar(s));
                 }
                 if (!ok) break;
                 ptx::mma_commit(accf_bar(b));        // the tile's accumulator is complete
             }
-            // Every MMA issued above must finish before TMEM is released.
+            // Every MMA issued above (and so every commit arrival it sends to
+            // the peers) must finish before TMEM is released.
             ptx::mma_commit(drain_bar);
             if (!ptx::wait_phase(drain_bar, 0)) atomicOr(status, kStatusTimeout);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= Cfg::EPI_WARP0) {
         // ------------------------------ epilogue ------------------------------
         const int q = warp - Cfg::EPI_WARP0;          // TMEM lane quarter (== warp % 4)
         const int et = 32 * q + lane;                 // epilogue thread: row of the tile
@@ -208,8 +273,9 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                 break;
             }
             ptx::tc_fence_after();
-            int tm, tn;
-            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tm, tn);
+            int tg, tn;
+            tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tg, tn);
+            const int tm = tg * CM + rank;
             const bool partial = item.kb0 > 0;                  // slabs of a tile owned earlier
             const bool owner = item.kb0 == 0 && item.kb1 < nk;  // adds later CTAs' partials
             int h_end = g + 1;
@@ -218,7 +284,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                 while (h_end < sched.sk_ctas && sk_start(sched, h_end) < tile_end) ++h_end;
                 bool ok = true;
                 for (int h = g + 1; h < h_end && ok; ++h)
-                    ok = __all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)h * 4 + q)) != 0;
+                    ok = __all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)(h * CM + rank) * 4 + q)) != 0;
                 if (!ok) {
                     if (lane == 0) atomicOr(status, kStatusTimeout);
                     break;
@@ -244,17 +310,18 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
 #pragma unroll
                 for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                 if (partial) {
-                    float4 *slot = reinterpret_cast<float4 *>(sched.partials + (int64_t)g * BM * BN);
+                    float4 *dst = reinterpret_cast<float4 *>(sched.partials + (int64_t)slot * BM * BN);
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        slot[((c0 + j) / 4) * 128 + et] = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        dst[((c0 + j) / 4) * 128 + et] = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
                     continue;
                 }
                 for (int h = g + 1; h < h_end; ++h) {
-                    const float4 *slot = reinterpret_cast<const float4 *>(sched.partials + (int64_t)h * BM * BN);
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(sched.partials + (int64_t)(h * CM + rank) * BM * BN);
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        const float4 p4 = slot[((c0 + j) / 4) * 128 + et];
+                        const float4 p4 = src[((c0 + j) / 4) * 128 + et];
                         f[j] += p4.x;
                         f[j + 1] += p4.y;
                         f[j + 2] += p4.z;
@@ -289,14 +356,26 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
             if (partial) {
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(sched.flags + (int64_t)g * 4 + q, 1u);
+                if (lane == 0) st_release_gpu(sched.flags + (int64_t)slot * 4 + q, 1u);
             }
         }
         ptx::tc_fence_before();
     }
 
     // ------------------------------ teardown ------------------------------
-    ptx::named_barrier(1, 32 * 5);                    // MMA warp + 4 epilogue warps
+    // Every role of this CTA is done: the producer has seen all bytes bound
+    // for this CTA land, the MMA warp has drained its MMAs and commits.
+    __syncthreads();
+    if constexpr (CM > 1) {
+        // No CTA leaves while a peer may still copy into its shared memory
+        // or arrive on its barriers: each tells every CTA of the cluster that
+        // it is done, then waits (bounded) until all have said so.
+        if (threadIdx.x == 0) {
+            for (int r = 0; r < CM; ++r) ptx::mbar_arrive_remote(exit_bar, (uint32_t)r);
+            if (!ptx::wait_phase(exit_bar, 0)) atomicOr(status, kStatusTimeout);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(taddr, Cfg::TMEM_COLS);
@@ -431,19 +510,25 @@ cudaError_t split_kmajor(const float *src, bool kmajor, int64_t rows, int64_t K,
     return cudaGetLastError();
 }
 
-using Tf32x3Wide = Tf32x3Cfg<256, 4>;    // 128 x 256 tiles, 4 stages of 48 KB
-using Tf32x3Square = Tf32x3Cfg<128, 6>;  // 128 x 128 tiles, 6 stages of 32 KB
+using Tf32x3Wide = Tf32x3Cfg<256, 4>;     // 128 x 256 tiles, 4 stages of 48 KB
+using Tf32x3Square = Tf32x3Cfg<128, 6>;   // 128 x 128 tiles, 6 stages of 32 KB
+using Tf32x3Pair = Tf32x3Cfg<256, 4, 2>;  // clusters of 2 CTAs sharing (multicasting) B tiles
 
+// The schedule runs over groups of CM vertically adjacent tiles, one group
+// per cluster; clusters of CM CTAs fill the SMs (every GB300 SM pair hosts
+// a cluster of 2).
 template <class Cfg>
 Schedule tf32x3_schedule(const GemmArgs &g, bool with_sk)
 {
-    return plan_schedule(g.M, g.N, g.K, Cfg::BM, Cfg::BN, Cfg::BK, g.num_sms, g.sched, with_sk);
+    return plan_schedule(g.M, g.N, g.K, Cfg::BM * Cfg::CM, Cfg::BN, Cfg::BK, g.num_sms / Cfg::CM, g.sched,
+                         with_sk);
 }
 
 template <class Cfg>
 size_t tf32x3_workspace(const GemmArgs &g)
 {
-    return tf32x3_layout(g).total + schedule_workspace_bytes(tf32x3_schedule<Cfg>(g, true), 4, Cfg::BM, Cfg::BN);
+    return tf32x3_layout(g).total +
+           schedule_workspace_bytes(tf32x3_schedule<Cfg>(g, true), 4 * Cfg::CM, Cfg::BM * Cfg::CM, Cfg::BN);
 }
 
 template <class Cfg>
@@ -479,14 +564,17 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     CUtensorMap mAh, mAl, mBh, mBl;
     if ((e = encode_kmajor(&mAh, a_hi, g.M, g.K, l.kp, Cfg::BM, Cfg::BK)) != cudaSuccess) return e;
     if ((e = encode_kmajor(&mAl, a_lo, g.M, g.K, l.kp, Cfg::BM, Cfg::BK)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Cfg::BN, Cfg::BK)) != cudaSuccess) return e;
-    if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Cfg::BN, Cfg::BK)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Cfg::B_PIECE_ROWS, Cfg::BK)) != cudaSuccess) return e;
+    if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Cfg::B_PIECE_ROWS, Cfg::BK)) != cudaSuccess) return e;
 
-    // Stream-K partials and flags follow the split operands in the workspace.
+    // Stream-K partials and flags (one slot and 4 flags per CTA) follow the
+    // split operands in the workspace.
+    constexpr int kFlags = 4 * Cfg::CM;
     Schedule sched = tf32x3_schedule<Cfg>(g, true);
-    if (sched.sk_ctas > 0 && g.workspace_bytes < l.total + schedule_workspace_bytes(sched, 4, Cfg::BM, Cfg::BN))
+    if (sched.sk_ctas > 0 &&
+        g.workspace_bytes < l.total + schedule_workspace_bytes(sched, kFlags, Cfg::BM * Cfg::CM, Cfg::BN))
         sched = tf32x3_schedule<Cfg>(g, false);
-    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, 4, stream)) != cudaSuccess)
+    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, kFlags, stream)) != cudaSuccess)
         return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
     float *C = g.C;
@@ -498,10 +586,28 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, false>);
     // Owners wait on other CTAs' partial sums: all CTAs must be resident.
-    if (sched.sk_ctas > 1)
-        e = cudaLaunchCooperativeKernel(fn, dim3(sched.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
-    else
-        e = cudaLaunchKernel(fn, dim3(sched.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (Cfg::CM > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = Cfg::CM;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (sched.sk_ctas > 1) {
+        attrs[na].id = cudaLaunchAttributeCooperative;
+        attrs[na].val.cooperative = 1;
+        ++na;
+    }
+    lc.gridDim = dim3((unsigned)(sched.grid * Cfg::CM));
+    lc.blockDim = dim3(Cfg::THREADS);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = attrs;
+    lc.numAttrs = (unsigned)na;
+    e = cudaLaunchKernelExC(&lc, fn, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -510,13 +616,17 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
 
 size_t tf32x3_workspace_bytes(int kernel, const GemmArgs &g)
 {
-    return kernel == kKernTf32x3_128x128 ? tf32x3_workspace<Tf32x3Square>(g) : tf32x3_workspace<Tf32x3Wide>(g);
+    if (kernel == kKernTf32x3_128x128) return tf32x3_workspace<Tf32x3Square>(g);
+    if (kernel == kKernTf32x3_pair) return tf32x3_workspace<Tf32x3Pair>(g);
+    return tf32x3_workspace<Tf32x3Wide>(g);
 }
 
 cudaError_t prepare_tf32x3()
 {
-    const cudaError_t e = prepare_cfg<Tf32x3Wide>();
-    return e != cudaSuccess ? e : prepare_cfg<Tf32x3Square>();
+    cudaError_t e = prepare_cfg<Tf32x3Wide>();
+    if (e == cudaSuccess) e = prepare_cfg<Tf32x3Square>();
+    if (e == cudaSuccess) e = prepare_cfg<Tf32x3Pair>();
+    return e;
 }
 
 cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream)
@@ -529,6 +639,7 @@ cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream)
         e.C = g.C + b * g.stride_c;
         e.batch = 1;
         const cudaError_t r = kernel == kKernTf32x3_128x128 ? launch_cfg<Tf32x3Square>(e, stream)
+                              : kernel == kKernTf32x3_pair  ? launch_cfg<Tf32x3Pair>(e, stream)
                                                             : launch_cfg<Tf32x3Wide>(e, stream);
         if (r != cudaSuccess) return r;
     }

@@ -130,6 +130,52 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same load delivered to every CTA of the cluster named in `mask`
+// (bit r = cluster rank r): each receives the box at the same shared-memory
+// offset `dst` and its bytes complete the mbarrier at the same offset `bar`.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                      int32_t x, int32_t y, uint16_t mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Number of CTAs in this CTA's cluster (1 without a cluster launch).
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+// All threads of all CTAs of the cluster (every thread must execute it).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// One arrival on the mbarrier at offset `bar` of the cluster's CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank)
+{
+    asm volatile("{\n\t.reg .b32 ra;\n\t"
+                 "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+                 "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
+                 "r"(rank)
+                 : "memory");
+}
+
 // L2 policy that keeps operand tiles resident: they are re-read by the CTAs
 // that compute the other tiles of the same block row or column.
 __device__ __forceinline__ uint64_t policy_evict_last()
@@ -201,6 +247,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes: thread i gets lane i.
+// tcgen05.commit whose arrival goes to the mbarrier at offset `bar` of
+// every CTA of the cluster in `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" ::"r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "

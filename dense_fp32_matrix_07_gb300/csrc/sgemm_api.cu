@@ -405,6 +405,7 @@ int sgemm_check_status(cudaStream_t stream)
             return SGEMM_ERR_CUDA;
         }
         if (word & kStatusTimeout) return SGEMM_ERR_TIMEOUT;
+        if (word & kStatusLaunchConfig) return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
 }

@@ -158,8 +158,10 @@ int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float 
  * sgemm_check_status — waits for `stream`, then reads and clears the current
  * device's error word. Returns SGEMM_ERR_TIMEOUT if any kernel of this
  * library on the device gave up a bounded wait since the last check (its
- * output is then incomplete), SGEMM_ERR_CUDA if the stream reports a CUDA
- * error, else SGEMM_OK. The error word is per device, not per stream.
+ * output is then incomplete), SGEMM_ERR_LAUNCH if a kernel found itself
+ * launched in a shape it cannot run in (a cluster kernel without its
+ * cluster; it then wrote nothing), SGEMM_ERR_CUDA if the stream reports a
+ * CUDA error, else SGEMM_OK. The error word is per device, not per stream.
  */
 int sgemm_check_status(cudaStream_t stream);
 

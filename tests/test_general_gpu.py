@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 
 IDS = sg.config_ids()
 CONFIGS = [-1, IDS["ffma2_128x128_k32_s4"], IDS["ffma2_128x256_k32_s4_sk"], IDS["ffma2_128x128_k32_s4_sk"],
-           IDS["ffma_128x128_k32_s4"], IDS["tf32x3_128x256_k16_s4"], IDS["tf32x3_128x256_k16_s4_sk"]]
+           IDS["ffma_128x128_k32_s4"], IDS["tf32x3_128x256_k16_s4"], IDS["tf32x3_128x256_k16_s4_sk"],
+           IDS["tf32x3_pair_128x256_k16_s4"]]
 CFG_IDS = ["auto" if c < 0 else sg.sgemm_config_name(c) for c in CONFIGS]
 
 

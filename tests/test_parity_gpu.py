@@ -189,12 +189,14 @@ def test_workload_sampled_check(cuda_device, oracle, name, dist):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("cfg_name", ["tf32x3_128x256_k16_s4", "tf32x3_pair_128x256_k16_s4"])
 @pytest.mark.parametrize("name", ["rect4097x3001x2049", "sq4096", "sq16384"])
-def test_tf32x3_tensor_core_path_at_full_size(cuda_device, oracle, name):
-    """The 3xTF32 tcgen05 path at the full workload sizes: sampled rows and
-    columns within 1e-4 * sum|A_ik B_kj| (float) and bit-exact (integers)."""
+def test_tf32x3_tensor_core_path_at_full_size(cuda_device, oracle, name, cfg_name):
+    """The 3xTF32 tcgen05 path at the full workload sizes (single CTAs, and
+    clusters of two sharing B tiles): sampled rows and columns within
+    1e-4 * sum|A_ik B_kj| (float) and bit-exact (integers)."""
     w = workloads.WORKLOADS[name]
-    cfg = sg.config_ids()["tf32x3_128x256_k16_s4"]
+    cfg = sg.config_ids()[cfg_name]
     for dist in (None, "int"):
         A, B, C = _run_workload(w, dist, config=cfg)
         r = _sampled_check(oracle, w, A, B, C, dist == "int")
