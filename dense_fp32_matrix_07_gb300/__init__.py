@@ -31,7 +31,8 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
-            "sgemm_test_withhold_copy", "sgemm_general", "sgemm_general_ex")
+            "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_general",
+            "sgemm_general_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +64,9 @@ def load(rebuild: bool = False):
             lib.sgemm_test_withhold_copy.restype = ctypes.c_int
             lib.sgemm_test_withhold_copy.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
                                                      _i64, ctypes.c_int, _vp]
+            lib.sgemm_test_launch_without_cluster.restype = ctypes.c_int
+            lib.sgemm_test_launch_without_cluster.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                                              _vp, _i64, _vp]
             gen = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
                    _vp, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _i64]
             lib.sgemm_general.restype = ctypes.c_int
@@ -116,6 +120,13 @@ def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) ->
     `slab`-th K slab, so the kernel's bounded waits expire (about a second)
     and sgemm_check_status() reports SGEMM_ERR_TIMEOUT."""
     return load().sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream)
+
+
+def sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """Test hook: the cluster-pair 3xTF32 configuration with its product
+    kernel launched without its 2-CTA cluster; the kernel detects it, does
+    nothing, and sgemm_check_status() reports SGEMM_ERR_LAUNCH."""
+    return load().sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def sgemm_general(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,

@@ -30,6 +30,7 @@ struct GemmArgs {
     void *workspace = nullptr;     // stream-K partial sums and flags, or null
     size_t workspace_bytes = 0;
     int withhold_it = -1;          // test hook: CTA 0's producer skips this copy
+    bool test_no_cluster = false;  // test hook: launch cluster kernels without their cluster
     // General form: C_b = alpha * A_b . B_b + beta * C_b for b < batch, with
     // batch strides in elements (a stride of 0 shares one operand).
     float alpha = 1.0f, beta = 0.0f;

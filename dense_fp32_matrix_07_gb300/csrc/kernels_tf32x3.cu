@@ -589,7 +589,7 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attrs[2];
     int na = 0;
-    if (Cfg::CM > 1) {
+    if (Cfg::CM > 1 && !g.test_no_cluster) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = Cfg::CM;
         attrs[na].val.clusterDim.y = 1;

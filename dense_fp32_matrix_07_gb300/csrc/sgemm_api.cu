@@ -192,6 +192,7 @@ struct Call {
     int config;          // -1: automatic
     int sched_override;  // -1: the configuration's policy (test knob)
     int withhold_it;     // -1: none (test knob)
+    bool no_cluster = false;  // test knob: cluster kernels launched without their cluster
 };
 
 // Elements spanned by `batch` entries of extent `e` at stride `s`, or -1.
@@ -257,6 +258,7 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
     g.sched = c.sched_override >= 0 ? c.sched_override : kConfigTable[cfg].sched;
     g.withhold_it = c.withhold_it;
+    g.test_no_cluster = c.no_cluster;
     g.alpha = c.alpha;
     g.beta = c.beta;
     g.batch = c.batch;
@@ -363,6 +365,14 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K, const float *A, in
     // Whole tiles: no stream-K waits between CTAs, only the withheld copy.
     return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, kSchedDataParallel,
                       slab < 0 ? -1 : slab, stream);
+}
+
+int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                      const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream)
+{
+    Call c{0, 0, M, N, K, 1.0f, A, lda, 0, B, ldb, 0, 0.0f, C, ldc, 0, 1, kCfgTf32x3_pair, -1, -1};
+    c.no_cluster = true;
+    return sgemm_call(c, stream);
 }
 
 int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha, const float *A,

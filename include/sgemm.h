@@ -214,6 +214,24 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K,
                              int slab, cudaStream_t stream);
 
 /*
+ * sgemm_test_launch_without_cluster — test hook for the launch-shape check
+ * of the cluster-pair 3xTF32 kernel (configuration
+ * "tf32x3_pair_128x256_k16_s4"; the pages have no counterpart).
+ *
+ * Runs that configuration, but launches its product kernel without the
+ * 2-CTA cluster it needs. The kernel's first action is to compare its
+ * cluster size with 2; finding 1, it sets the device error word and returns
+ * without touching shared memory, barriers or C. The call returns SGEMM_OK
+ * (the launch itself succeeds), sgemm_check_status() then returns
+ * SGEMM_ERR_LAUNCH, and C is unchanged. Arguments as sgemm() (the split
+ * pre-passes still run into library-owned scratch).
+ */
+int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
+                                      const float *A, int64_t lda,
+                                      const float *B, int64_t ldb,
+                                      float *C, int64_t ldc, cudaStream_t stream);
+
+/*
  * sgemm_noalloc — sgemm() for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for users of
