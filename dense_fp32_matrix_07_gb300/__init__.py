@@ -116,7 +116,7 @@ def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 
 
 def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) -> int:
-    """Test hook: sgemm() whose first CTA never issues the copy of its
+    """Test hook: the 128x256 TMA product whose first CTA never issues the copy of its
     `slab`-th K slab, so the kernel's bounded waits expire (about a second)
     and sgemm_check_status() reports SGEMM_ERR_TIMEOUT."""
     return load().sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream)

@@ -44,7 +44,10 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
         sk = true;
     } else if (with_sk && policy == kSchedAuto) {
         const int64_t rounds = (s.tiles + slots - 1) / slots;
-        sk = (double)s.tiles < 0.97 * (double)(rounds * slots) && s.nk >= 8;
+        // Whole tiles unless the last wave is less than 90 % full (at 1536^3
+        // on 128 x 128 tiles, 144 tiles on 152 SMs, whole tiles measured
+        // 123.1 us against 126.1 us with the stream-K tail).
+        sk = (double)s.tiles < 0.90 * (double)(rounds * slots) && s.nk >= 8;
     }
     if (!sk) return s;
     const int64_t full_rounds = s.tiles / slots;

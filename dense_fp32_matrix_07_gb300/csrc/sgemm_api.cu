@@ -250,7 +250,10 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     }
 
     const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, dev->num_sms};
-    const int cfg = c.config < 0 ? select_config(p) : c.config;
+    int cfg = c.config < 0 ? select_config(p) : c.config;
+    // The automatic choice for tiny products is the plain-form-only tiled
+    // kernel; the general form takes the smallest TMA tiles instead.
+    if (c.config < 0 && !plain && !kConfigTable[cfg].uses_tma) cfg = kCfgFfma2_128x64;
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
     // Kernels without TMA (the simple and ladder kernels) run the plain form only.
     if (!plain && !kConfigTable[cfg].uses_tma) return SGEMM_ERR_UNSUPPORTED;
@@ -362,8 +365,9 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K, const float *A, in
                              const float *B, int64_t ldb, float *C, int64_t ldc, int slab,
                              cudaStream_t stream)
 {
-    // Whole tiles: no stream-K waits between CTAs, only the withheld copy.
-    return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, kSchedDataParallel,
+    // The 128x256 TMA kernel (whatever the size) on whole tiles: no stream-K
+    // waits between CTAs, only the withheld copy.
+    return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, kCfgFfma2_128x256, kSchedDataParallel,
                       slab < 0 ? -1 : slab, stream);
 }
 

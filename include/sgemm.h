@@ -197,13 +197,15 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K,
  *
  * Failure detection ("Перемножение матриц: наивное и тайловое", section 2:
  * a tile may be used only once it is fully loaded; here that wait is
- * bounded). Runs sgemm() with whole-tile scheduling, except that the producer
+ * bounded). Runs the product on the 128x256 TMA configuration
+ * ("ffma2_128x256_k32_s4") with whole-tile scheduling, whatever the size,
+ * except that the producer
  * of the first CTA never issues the copy of its `slab`-th K slab, so the
  * consumers' wait for it can never be satisfied. Every device-side wait gives
  * up after about a second; the kernel then sets the device error word and
  * exits without faulting, the context stays usable, and sgemm_check_status()
  * returns SGEMM_ERR_TIMEOUT. C is left incomplete. The call takes about one
- * to two seconds on the GPU. slab < 0 behaves like sgemm() (whole tiles).
+ * to two seconds on the GPU. slab < 0 computes the product normally.
  * Arguments otherwise as sgemm(); aligned operands make the kernel read A and
  * B in place (no packing) so the withheld copy is the product's own.
  */

@@ -80,19 +80,31 @@ def test_plan_packs_only_misaligned_operands():
     rc, cfg, pa, pb = sg.sgemm_plan(4097, 3001, 2049, 2049, 3001, 3001, 0, 0, 0, 148)
     assert rc == 0 and (pa, pb) == (1, 1)
     # A misaligned base address alone forces a pack of that operand.
-    rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 4, 0, 0, 148)
+    rc, cfg, pa, pb = sg.sgemm_plan(1024, 1024, 1024, 1024, 1024, 1024, 4, 0, 0, 148)
     assert rc == 0 and (pa, pb) == (1, 0)
-    rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 0, 8, 12, 148)
+    rc, cfg, pa, pb = sg.sgemm_plan(1024, 1024, 1024, 1024, 1024, 1024, 0, 8, 12, 148)
     assert rc == 0 and (pa, pb) == (0, 1)
+    # The simple tiled kernel (tiny products) reads any layout in place.
+    rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 4, 8, 12, 148)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == "tiled16_simple" and (pa, pb) == (0, 0)
 
 
-def test_plan_picks_smaller_tiles_when_the_grid_would_be_underfilled():
-    rc, big, *_ = sg.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, 0, 0, 0, 148)
-    rc2, small, *_ = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 0, 0, 0, 148)
-    assert rc == rc2 == 0
-    assert big != small
-    assert sg.sgemm_config_name(big).startswith("ffma")
-    assert sg.sgemm_config_name(small).startswith("ffma")
+@pytest.mark.parametrize("n,name", [
+    (256, "tiled16_simple"),            # tiny: no TMA set-up
+    (384, "ffma2_128x64_k32_s4"),       # 9 tiles of 128x128: the smallest TMA tiles
+    (1024, "ffma2_128x128_k32_s4"),     # 64 tiles of 128x128 (>= a third of the SMs)
+    (2048, "ffma2_128x128_k32_s4"),     # 128 tiles of 128x256 < 148 SMs
+    (4096, "ffma2_128x256_k32_s4"),     # 512 tiles of 128x256
+])
+def test_plan_tile_size_follows_the_problem(n, name):
+    rc, cfg, *_ = sg.sgemm_plan(n, n, n, n, n, n, 0, 0, 0, 148)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == name
+
+
+def test_plan_long_k_skips_the_simple_kernel():
+    # A tiny output with a long K goes to the stream-K kernel, not one 16x16 block.
+    rc, cfg, *_ = sg.sgemm_plan(1, 1, 1 << 20, 1 << 20, 1, 1, 0, 0, 0, 148)
+    assert rc == 0 and sg.sgemm_config_name(cfg).startswith("ffma")
 
 
 def test_plan_rejects_nonpositive_sm_count():
