@@ -2,6 +2,7 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload NAME] [--config ID]
+                [--op-a 0|1] [--op-b 0|1] [--alpha X] [--beta Y] [--batch B]
 
 A step is one C = A . B product of the workload (default: the 4096-cube,
 N(0,1) inputs, seed 2) through the library's C ABI, inputs resident in HBM.
@@ -28,6 +29,12 @@ Also reported on the same JSON line:
                 every step), the same steps back to back without the flush;
   clocks        nvidia-smi samples taken during the timed region.
 --impl reference times that oracle alone as the reference arm.
+
+With --op-a/--op-b/--alpha/--beta/--batch the step is instead one call of
+the general form C_b = alpha * op(A_b) . op(B_b) + beta * C_b over `batch`
+copies of the workload's operands (stored transposed where op = 1), FLOPs
+batch * 2*M*N*K; the step includes any packing pass the call makes. The
+host-buffer, tensor-core and CPU legs are then left out.
 """
 
 from __future__ import annotations
@@ -372,6 +379,13 @@ def main():
                     help="skip the separately reported 3xTF32 tensor-core measurement")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="oracle threads for cpu_baseline (default: all host cores)")
+    ap.add_argument("--op-a", type=int, choices=(0, 1), default=0,
+                    help="general form: A stored transposed (K x M)")
+    ap.add_argument("--op-b", type=int, choices=(0, 1), default=0,
+                    help="general form: B stored transposed (N x K)")
+    ap.add_argument("--alpha", type=float, default=1.0, help="general form: alpha")
+    ap.add_argument("--beta", type=float, default=0.0, help="general form: beta (C is read when nonzero)")
+    ap.add_argument("--batch", type=int, default=1, help="general form: strided batch of this many products")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -397,29 +411,63 @@ def main():
 
     w = workloads.WORKLOADS[args.workload]
     A, B = workloads.make_workload(w)
-    dA, dB = A.to(dev), B.to(dev)
-    dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    rc, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(),
-                                    dB.data_ptr(), dC.data_ptr(), num_sms)
+    general = args.op_a or args.op_b or args.alpha != 1.0 or args.beta != 0.0 or args.batch > 1
+    if general:
+        # The host-buffer, tensor-core and CPU legs belong to the plain workload.
+        args.no_e2e = args.no_tf32x3 = args.no_cpu_baseline = True
+    if not general:
+        dA, dB = A.to(dev), B.to(dev)
+        dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
+        rc, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(),
+                                        dB.data_ptr(), dC.data_ptr(), num_sms)
+        launches_per_step = 1 + pa + pb
+        total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
+        flops = product_flops(w.M, w.N, w.K)
+
+        def step():
+            r = sg.sgemm_ex(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
+                            dC.data_ptr(), w.ldc, args.config, sh)
+            if r != 0:
+                raise RuntimeError(sg.sgemm_error_string(r))
+    else:
+        # The general form C_b = alpha * op(A_b) . op(B_b) + beta * C_b over
+        # `batch` copies of the workload's operands, stored as op asks (A as
+        # K x M when op_a = 1, B as N x K when op_b = 1) with tight strides.
+        gA = (A[:, :w.K].t() if args.op_a else A[:, :w.K]).contiguous()
+        gB = (B[:, :w.N].t() if args.op_b else B[:, :w.N]).contiguous()
+        lda_g, ldb_g, ldc_g = gA.shape[1], gB.shape[1], w.N
+        sa, sb, sc = gA.numel(), gB.numel(), w.M * w.N
+        dA = gA.reshape(1, -1).to(dev).repeat(args.batch, 1)
+        dB = gB.reshape(1, -1).to(dev).repeat(args.batch, 1)
+        dC = torch.ones((args.batch, w.M, w.N), dtype=torch.float32, device=dev)
+        cfg = args.config
+        if cfg < 0:
+            rc, cfg, _, _ = sg.sgemm_plan(w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, num_sms)
+            if not sg.sgemm_config_name(cfg).startswith(("ffma", "tf32")):
+                cfg = sg.config_ids()["ffma2_128x64_k32_s4"]     # the general form's choice for tiny products
+        packs = sg.sgemm_config_name(cfg).startswith("ffma")
+        pa = int(packs and (args.op_a == 1 or lda_g % 4 != 0))
+        pb = int(packs and (args.op_b == 1 or ldb_g % 4 != 0))
+        launches_per_step = (1 + pa + pb) if packs else 3 * args.batch
+        total_bytes = 4 * args.batch * (sa + sb + sc)
+        flops = args.batch * product_flops(w.M, w.N, w.K)
+
+        def step():
+            r = sg.sgemm_general_ex(args.op_a, args.op_b, w.M, w.N, w.K, args.alpha, dA.data_ptr(), lda_g, sa,
+                                    dB.data_ptr(), ldb_g, sb, args.beta, dC.data_ptr(), ldc_g, sc, args.batch,
+                                    args.config, sh)
+            if r != 0:
+                raise RuntimeError(sg.sgemm_error_string(r))
     if args.config >= 0:
         cfg = args.config
     cfg_name = sg.sgemm_config_name(cfg)
-    launches_per_step = 1 + pa + pb
-    flops = product_flops(w.M, w.N, w.K)
 
-    total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
     flush = None
     if total_bytes <= L2_BYTES:
         flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        r = sg.sgemm_ex(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
-                        dC.data_ptr(), w.ldc, args.config, sh)
-        if r != 0:
-            raise RuntimeError(sg.sgemm_error_string(r))
 
     for _ in range(args.warmup):
         step()
@@ -615,7 +663,7 @@ def main():
     peak_tflops = num_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     avg_launch_s = statistics.mean(kernel_ms) / 1e3
     achieved_tflops = flops / avg_launch_s / 1e12
-    traffic = profiled_traffic(cfg_name)
+    traffic = None if general else profiled_traffic(cfg_name)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -629,7 +677,11 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": workload_config(w, cfg_name),
+        "config": workload_config(w, cfg_name) if not general else dict(
+            workload_config(w, cfg_name, l2=(f"A+B+C = {total_bytes / 1e6:.1f} MB"
+                                             + (": L2 flushed between steps" if flush is not None else " > L2, no flush"))),
+            form={"op_a": args.op_a, "op_b": args.op_b, "alpha": args.alpha, "beta": args.beta,
+                  "batch": args.batch}),
         "fp32_peak_pct": round(100.0 * value / world / 1e3 / peak_tflops, 2),
         "e2e": None if e2e_value is None else {"value": round(e2e_value, 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
