@@ -152,30 +152,41 @@ __global__ void pack_batched_kernel(const float *__restrict__ src, int64_t rows,
 }
 
 // dst[b * s_dst + c * ld_dst + r] = src[b * s_src + r * ld_src + c], through
-// 32 x 32 shared-memory tiles so reads and writes are both coalesced.
-__global__ void pack_transpose_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
-                                              int64_t ld_src, int64_t s_src, float *__restrict__ dst,
-                                              int64_t ld_dst, int64_t s_dst, int64_t batch)
+// 64 x 64 shared-memory tiles (padded by one column): 32 x 8 threads, each
+// moving 16 elements per tile, so reads (along c) and writes (along r) are
+// both 128-byte warp segments.
+__global__ void __launch_bounds__(256)
+pack_transpose_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
+                              int64_t ld_src, int64_t s_src, float *__restrict__ dst,
+                              int64_t ld_dst, int64_t s_dst, int64_t batch)
 {
-    __shared__ float tile[32][33];
+    __shared__ float tile[64][65];
     const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8 threads
-    const int64_t tiles_c = (cols + 31) / 32;
-    const int64_t per_entry = ((rows + 31) / 32) * tiles_c;
+    const int64_t tiles_c = (cols + 63) / 64;
+    const int64_t per_entry = ((rows + 63) / 64) * tiles_c;
     for (int64_t t = blockIdx.x; t < batch * per_entry; t += gridDim.x) {
         const int64_t b = t / per_entry, tt = t % per_entry;
-        const int64_t r0 = (tt / tiles_c) * 32, c0 = (tt % tiles_c) * 32;
+        const int64_t r0 = (tt / tiles_c) * 64, c0 = (tt % tiles_c) * 64;
         const float *sb = src + b * s_src;
         float *db = dst + b * s_dst;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
-            tile[ty + 8 * i][tx] = (r < rows && c < cols) ? sb[r * ld_src + c] : 0.0f;
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = r0 + ty + 8 * i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = c0 + tx + 32 * h;
+                tile[ty + 8 * i][tx + 32 * h] = (r < rows && c < cols) ? sb[r * ld_src + c] : 0.0f;
+            }
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;
-            if (c < cols && r < rows) db[c * ld_dst + r] = tile[tx][ty + 8 * i];
+        for (int i = 0; i < 8; ++i) {
+            const int64_t c = c0 + ty + 8 * i;   // output row
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t r = r0 + tx + 32 * h;
+                if (c < cols && r < rows) db[c * ld_dst + r] = tile[tx + 32 * h][ty + 8 * i];
+            }
         }
         __syncthreads();
     }
@@ -218,7 +229,7 @@ cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_
                                           int64_t ld_dst, int64_t s_dst, int64_t batch,
                                           cudaStream_t stream)
 {
-    const int64_t tiles = batch * ((rows + 31) / 32) * ((cols + 31) / 32);
+    const int64_t tiles = batch * ((rows + 63) / 64) * ((cols + 63) / 64);
     pack_transpose_batched_kernel<<<grid_for(tiles, 1, 8192), dim3(32, 8), 0, stream>>>(
         src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch);
     return cudaGetLastError();

@@ -417,32 +417,41 @@ tf32_split_rows_kernel(const float *__restrict__ src, int64_t rows, int64_t cols
 }
 
 // The same split of B (K x N, leading dimension ld), written transposed:
-// hiT[n * ldo + k], loT[n * ldo + k]. 32 x 32 tiles through shared memory so
-// both the reads (along n) and the writes (along k) are coalesced.
-__global__ void tf32_split_transpose_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
-                                            int64_t ld, float *__restrict__ hiT, float *__restrict__ loT,
-                                            int64_t ldo)
+// hiT[n * ldo + k], loT[n * ldo + k]. 64 x 64 tiles through shared memory
+// (padded by one column), 32 x 8 threads moving 16 elements each, so both
+// the reads (along n) and the writes (along k) are 128-byte warp segments.
+__global__ void __launch_bounds__(256)
+tf32_split_transpose_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t ld,
+                            float *__restrict__ hiT, float *__restrict__ loT, int64_t ldo)
 {
-    __shared__ float tile[32][33];
+    __shared__ float tile[64][65];
     const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8 threads
-    const int64_t tiles_c = (cols + 31) / 32;
-    const int64_t ntiles = ((rows + 31) / 32) * tiles_c;
+    const int64_t tiles_c = (cols + 63) / 64;
+    const int64_t ntiles = ((rows + 63) / 64) * tiles_c;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int64_t r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+        const int64_t r0 = (t / tiles_c) * 64, c0 = (t % tiles_c) * 64;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
-            tile[ty + 8 * i][tx] = (r < rows && c < cols) ? src[r * ld + c] : 0.0f;
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = r0 + ty + 8 * i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = c0 + tx + 32 * h;
+                tile[ty + 8 * i][tx + 32 * h] = (r < rows && c < cols) ? src[r * ld + c] : 0.0f;
+            }
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;   // output row c, column r
-            if (c < cols && r < rows) {
-                const float x = tile[tx][ty + 8 * i];
-                const float h = ptx::to_tf32(x);
-                hiT[c * ldo + r] = h;
-                loT[c * ldo + r] = ptx::to_tf32(x - h);
+        for (int i = 0; i < 8; ++i) {
+            const int64_t c = c0 + ty + 8 * i;   // output row c, column r
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t r = r0 + tx + 32 * h;
+                if (c < cols && r < rows) {
+                    const float x = tile[tx + 32 * h][ty + 8 * i];
+                    const float xh = ptx::to_tf32(x);
+                    hiT[c * ldo + r] = xh;
+                    loT[c * ldo + r] = ptx::to_tf32(x - xh);
+                }
             }
         }
         __syncthreads();
@@ -503,8 +512,8 @@ cudaError_t split_kmajor(const float *src, bool kmajor, int64_t rows, int64_t K,
         else
             tf32_split_rows_kernel<false><<<grid, 256, 0, stream>>>(src, rows, K, ld, hi, lo, kp);
     } else {
-        const int64_t tiles = ((K + 31) / 32) * ((rows + 31) / 32);
-        const unsigned grid = (unsigned)(tiles < (int64_t)num_sms * 32 ? tiles : (int64_t)num_sms * 32);
+        const int64_t tiles = ((K + 63) / 64) * ((rows + 63) / 64);
+        const unsigned grid = (unsigned)(tiles < (int64_t)num_sms * 16 ? tiles : (int64_t)num_sms * 16);
         tf32_split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(src, K, rows, ld, hi, lo, kp);
     }
     return cudaGetLastError();
