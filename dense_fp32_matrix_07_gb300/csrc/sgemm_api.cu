@@ -11,8 +11,9 @@
 
 namespace sgemm_gb300 {
 
-// Device error word: kernels OR status bits into it (kStatusTimeout), and
-// sgemm_check_status() reads and clears it. One copy exists per device.
+// Device error word: kernels OR status bits into it (kStatusTimeout,
+// kStatusLaunchConfig), and sgemm_check_status() reads and clears it. One
+// copy exists per device.
 __device__ unsigned int g_status_word;
 
 namespace {
@@ -147,7 +148,7 @@ const char *sgemm_error_string(int code)
     case SGEMM_ERR_INVALID_VALUE: return "SGEMM_ERR_INVALID_VALUE: invalid size, leading dimension, pointer, overlap or config";
     case SGEMM_ERR_OVERFLOW: return "SGEMM_ERR_OVERFLOW: an index or byte offset would overflow";
     case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: scratch allocation failed";
-    case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: kernel launch failed";
+    case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: a kernel launch failed, or a kernel found its launch shape wrong and did nothing";
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a device-side wait hit its spin limit";
     case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: CUDA runtime failure";
     case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: the forced config cannot run this problem";

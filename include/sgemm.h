@@ -56,7 +56,10 @@ enum {
                                     or a size exceeds the kernels' 2^31-1
                                     coordinate range */
     SGEMM_ERR_ALLOC = 3,         /* scratch allocation failed */
-    SGEMM_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError) */
+    SGEMM_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError), or, from
+                                    sgemm_check_status(), a kernel found its launch shape
+                                    wrong (a cluster kernel without its cluster) and did
+                                    nothing */
     SGEMM_ERR_TIMEOUT = 5,       /* a device-side wait hit its bounded spin
                                     limit; reported by sgemm_check_status() */
     SGEMM_ERR_CUDA = 6,          /* another CUDA runtime failure (no device,
