@@ -30,6 +30,9 @@ Also reported on the same JSON line:
   clocks        nvidia-smi samples taken during the timed region.
 --impl reference times that oracle alone as the reference arm.
 
+--probe-fma runs the FP32 FMA throughput probes (FLOP per clock per SM of the
+mainloop's instruction patterns: the ceiling of the main kernel) and exits.
+
 With --op-a/--op-b/--alpha/--beta/--batch the step is instead one call of
 the general form C_b = alpha * op(A_b) . op(B_b) + beta * C_b over `batch`
 copies of the workload's operands (stored transposed where op = 1), FLOPs
@@ -364,6 +367,39 @@ def cpu_baseline(w, A, B, threads=0, budget_s=30.0, min_s=10.0):
             "sample": f"{what} x {reps}, {dt:.1f} s"}
 
 
+FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_registers",
+              "ffma2_outer_8x8_registers_fixed", "ffma2_outer_8x8_registers_rotating",
+              "sgemm_inner_loop_8x8_smem", "sgemm_inner_loop_8x16_smem")
+
+
+def run_fma_probe():
+    """The FP32 FMA throughput probes (dense_fp32_matrix_07_gb300/probe/
+    fma_ceiling.cu): FLOP per clock per SM of each mainloop pattern, against
+    the nominal 128 lanes x 2 FLOP; one JSON line."""
+    import ctypes
+    from dense_fp32_matrix_07_gb300 import build as _b
+    _b.build()
+    lib = ctypes.CDLL(_b.PROBE_LIB)
+    lib.fma_probe_run.restype = ctypes.c_int
+    d = ctypes.c_double
+    lib.fma_probe_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(d), ctypes.POINTER(d),
+                                  ctypes.POINTER(d)]
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = {}
+    for kind, name in enumerate(FMA_PROBES):
+        ms, mhz, flops = d(), d(), d()
+        rc = lib.fma_probe_run(kind, 5, ctypes.byref(ms), ctypes.byref(mhz), ctypes.byref(flops))
+        if rc != 0:
+            raise RuntimeError(f"probe {name}: CUDA error {rc}")
+        per_clk = flops.value / (ms.value * 1e-3) / (mhz.value * 1e6) / sms
+        out[name] = {"best_ms": round(ms.value, 4), "sm_mhz": round(mhz.value, 1),
+                     "flop_per_clk_per_sm": round(per_clk, 1), "frac_of_256": round(per_clk / 256.0, 4)}
+    print(json.dumps({"probe": "fp32_fma_ceiling", "sms": sms, "nominal_flop_per_clk_per_sm": 256,
+                      "results": out}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,6 +422,8 @@ def main():
     ap.add_argument("--alpha", type=float, default=1.0, help="general form: alpha")
     ap.add_argument("--beta", type=float, default=0.0, help="general form: beta (C is read when nonzero)")
     ap.add_argument("--batch", type=int, default=1, help="general form: strided batch of this many products")
+    ap.add_argument("--probe-fma", action="store_true",
+                    help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -393,6 +431,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.probe_fma:
+        return run_fma_probe()
 
     import torch
     import dense_fp32_matrix_07_gb300 as sg

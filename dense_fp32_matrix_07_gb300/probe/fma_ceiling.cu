@@ -1,0 +1,289 @@
+// FP32 FMA throughput probes: what the FP32 pipe of one GB300 SM sustains
+// for the instruction patterns an SGEMM mainloop is made of. They bound the
+// main kernel's roofline from the inside (the nominal peak is 128 FMA lanes
+// x 2 FLOP per clock per SM; Chapter 9: Optimised Matrix Multiplication,
+// section 9.5, counts the per-SM FP32 lanes the same way).
+//
+// Every probe runs one block per SM, touches only its own output slot and a
+// shared-memory tile it fills itself, and has no waits; it measures its own
+// SM clock (clock64 over %globaltimer) so FLOP per clock per SM follows.
+//
+//   0  FFMA, loop-invariant multiplicands, 16 independent chains per thread
+//   1  FFMA2 (paired FP32 FMA), loop-invariant multiplicands
+//   2  FFMA, 8 x 8 outer product from registers (a[i] * b[j] into acc[i][j])
+//   3  FFMA2, 8 x 8 outer product from registers, a[i] broadcast to both
+//      lanes, fixed operand registers
+//   4  as 3, with the operand registers rotated every k
+//   5  SGEMM inner loop from shared memory: 8 x 8 thread tiles, 128 x 128
+//      block, A rows 128-byte swizzled (LDS.128 of 4 k), B read as float4
+//   6  as 5 with 8 x 16 thread tiles (128 x 256 block): the main kernel's tile
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+namespace {
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record(unsigned long long *clk, long long c0, unsigned long long t0)
+{
+    const long long c1 = clock64();
+    const unsigned long long t1 = global_ns();
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        clk[0] = (unsigned long long)(c1 - c0);
+        clk[1] = t1 - t0;
+    }
+}
+
+// 0 / 1: loop-invariant multiplicands.
+template <bool PAIRED>
+__global__ void __launch_bounds__(256) peak_kernel(float *out, int iters, float x, float y, unsigned long long *clk)
+{
+    float2 a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = make_float2(threadIdx.x * 1e-3f + j, j * 0.5f);
+    const float2 x2 = make_float2(x, x), y2 = make_float2(y, y);
+    const long long c0 = clock64();
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (PAIRED) {
+                a[j] = __ffma2_rn(a[j], x2, y2);
+            } else {
+                a[j].x = fmaf(a[j].x, x, y);
+                a[j].y = fmaf(a[j].y, x, y);
+            }
+        }
+    }
+    record(clk, c0, t0);
+    float s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += a[j].x + a[j].y;
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+// 2 / 3 / 4: 8 x 8 outer products from registers, 32 k per iteration.
+template <int MODE>
+__global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, unsigned long long *clk)
+{
+    float a[8], bs[8];
+    float2 b[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a[i] = threadIdx.x * 1e-3f + i;
+        bs[i] = i * 0.3f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = make_float2(q * 0.5f, q * 0.25f + threadIdx.x * 1e-4f);
+    float2 acc[8][4];
+    float accs[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) accs[i][j] = 0.f;
+    }
+    const long long c0 = clock64();
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (MODE == 2) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) accs[i][j] = fmaf(a[i], bs[j], accs[i][j]);
+                } else if (MODE == 3) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+                } else {
+                    const float av = a[(i + k) & 7];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        acc[i][q] = __ffma2_rn(make_float2(av, av), b[(q + k) & 3], acc[i][q]);
+                }
+            }
+        }
+    }
+    record(clk, c0, t0);
+    float s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s += acc[i][q].x + acc[i][q].y;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += accs[i][j];
+    }
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+}  // namespace
+
+namespace {
+
+// 5 / 6: the SGEMM inner loop on one 32-deep slab held in shared memory.
+// 8 warps as 2 x 4, each 8 x 4 threads with TM x TN thread tiles: block
+// 128 x (16 TN). A is [128][32] floats with 16-byte chunk c of row r stored
+// at chunk c ^ (r & 7); B is [32][BN] floats. Each thread loads 4 k of A per
+// row with one LDS.128 and TN/4 float4 of B per k, then issues TM * TN / 2
+// broadcast FFMA2 per k.
+template <int TN>
+__global__ void __launch_bounds__(256, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
+{
+    constexpr int TM = 8, TR = 8, TC = 4, WN = 4;
+    constexpr int BM = 128, BN = WN * TC * TN;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float *sA = reinterpret_cast<float *>(smem);
+    float *sB = reinterpret_cast<float *>(smem + BM * 128);
+    for (int e = threadIdx.x; e < BM * 32; e += 256) sA[e] = (e % 7) * 0.25f - 0.5f;
+    for (int e = threadIdx.x; e < BN * 32; e += 256) sB[e] = (e % 5) * 0.125f - 0.25f;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wm = (warp / WN) * TR * TM, wn = (warp % WN) * TC * TN;
+    const int ty = lane / TC, tx = lane % TC;
+    const char *As = reinterpret_cast<const char *>(sA) + (wm + ty) * 128;
+    const char *Bs = reinterpret_cast<const char *>(sB) + (wn + tx * 4) * 4;
+    float2 acc[TM][TN / 2];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+    const long long c0 = clock64();
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < iters; ++it) {
+        // An opaque zero offset keeps the compiler from hoisting the shared
+        // loads out of the iteration loop.
+        unsigned z;
+        asm volatile("mov.u32 %0, 0;" : "=r"(z));
+        const char *Ai = As + z, *Bi = Bs + z;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            float a[TM][4];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const int r = ty + TR * i;    // (wm + r) & 7 == r & 7
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(Ai + TR * i * 128 + (((unsigned)kb ^ (unsigned)(r & 7)) << 4));
+                a[i][0] = v.x;
+                a[i][1] = v.y;
+                a[i][2] = v.z;
+                a[i][3] = v.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int k = kb * 4 + kk;
+                float4 b[TN / 4];
+#pragma unroll
+                for (int g = 0; g < TN / 4; ++g)
+                    b[g] = *reinterpret_cast<const float4 *>(Bi + k * BN * 4 + g * TC * 16);
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const float2 aa = make_float2(a[i][kk], a[i][kk]);
+#pragma unroll
+                    for (int g = 0; g < TN / 4; ++g) {
+                        acc[i][2 * g] = __ffma2_rn(aa, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
+                        acc[i][2 * g + 1] = __ffma2_rn(aa, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+                    }
+                }
+            }
+        }
+    }
+    record(clk, c0, t0);
+    float s = 0;
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) s += acc[i][j].x + acc[i][j].y;
+    out[blockIdx.x * 256 + threadIdx.x] = s;
+}
+
+template <int TN>
+constexpr int inner_smem() { return 128 * 128 + 4 * 4 * TN * 128; }
+
+}  // namespace
+
+extern "C" {
+
+// Number of probe kinds (see the list at the top of this file).
+int fma_probe_count(void) { return 7; }
+
+// Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
+// timed launches (CUDA events); returns the best launch time, the SM clock
+// the kernel measured (MHz) and the FP32 operations of one launch (FMA = 2).
+// Returns 0, or a cudaError_t value. Allocates and frees its own small
+// buffers; synchronises the device.
+int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *flops)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    if (kind < 0 || kind > 6 || reps < 1) return (int)cudaErrorInvalidValue;
+    float *out = nullptr;
+    unsigned long long *clk = nullptr;
+    if ((e = cudaMalloc(&out, sizeof(float) * 256 * (size_t)sms)) != cudaSuccess) return (int)e;
+    if ((e = cudaMalloc(&clk, 2 * sizeof(unsigned long long))) != cudaSuccess) {
+        cudaFree(out);
+        return (int)e;
+    }
+    const int peak_iters = 1 << 16, loop_iters = 2048;
+    double f = 0;
+    auto launch = [&]() {
+        switch (kind) {
+        case 0: peak_kernel<false><<<sms, 256>>>(out, peak_iters, 0.999f, 0.001f, clk); break;
+        case 1: peak_kernel<true><<<sms, 256>>>(out, peak_iters, 0.999f, 0.001f, clk); break;
+        case 2: outer_kernel<2><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 3: outer_kernel<3><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 4: outer_kernel<4><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 5: inner_kernel<8><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
+        default: inner_kernel<16><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        }
+    };
+    if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
+    else if (kind <= 4) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
+    else if (kind == 5) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
+    else f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<16>());
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    std::vector<float> ms;
+    if (e == cudaSuccess) {
+        launch();
+        e = cudaDeviceSynchronize();
+    }
+    for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+        cudaEventRecord(e0);
+        launch();
+        cudaEventRecord(e1);
+        e = cudaEventSynchronize(e1);
+        float t = 0;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+        ms.push_back(t);
+    }
+    unsigned long long c[2] = {0, 0};
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpy(c, clk, sizeof(c), cudaMemcpyDeviceToHost);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(out);
+    cudaFree(clk);
+    if (e != cudaSuccess) return (int)e;
+    *best_ms = *std::min_element(ms.begin(), ms.end());
+    *sm_mhz = c[1] ? (double)c[0] / (double)c[1] * 1e3 : 0.0;
+    *flops = f;
+    return 0;
+}
+
+}  // extern "C"

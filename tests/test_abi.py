@@ -110,3 +110,15 @@ def test_plan_long_k_skips_the_simple_kernel():
 def test_plan_rejects_nonpositive_sm_count():
     rc, *_ = sg.sgemm_plan(4, 4, 4, 4, 4, 4, 0, 0, 0, 0)
     assert rc == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_fma_probe_library_exports_its_entry_points():
+    # The measurement-only probe library is built beside libsgemm.so and
+    # loads without a GPU; its functions are only called on one.
+    from dense_fp32_matrix_07_gb300 import build as _b
+    _b.build()
+    lib = ctypes.CDLL(_b.PROBE_LIB)
+    assert hasattr(lib, "fma_probe_run") and hasattr(lib, "fma_probe_count")
+    lib.fma_probe_count.restype = ctypes.c_int
+    import bench
+    assert lib.fma_probe_count() == len(bench.FMA_PROBES)
