@@ -27,12 +27,15 @@
  * Layout: all matrices are row-major FP32 in device memory (HBM).
  * Ownership: every pointer is caller-owned device memory; the library never
  * frees, retains or reads host memory through it. Scratch space the library
- * needs (a packed copy of an operand whose rows are not 16-byte aligned) is
- * taken from a library-owned, stream-ordered memory pool on `stream` and
- * returned on `stream`; it is never exposed.
+ * needs (a packed copy of an operand whose rows are not 16-byte aligned, the
+ * partial sums and flags of a stream-K tail, the hi/lo operand planes of the
+ * 3xTF32 configurations) is taken from a library-owned, stream-ordered
+ * memory pool on `stream` and returned on `stream`; it is never exposed.
  * Asynchrony: calls return after enqueueing work on `stream`; results are
- * ready when the stream's work completes. A call enqueues at most three
- * kernels (operand packing, then the product) and no host synchronisation.
+ * ready when the stream's work completes. An FFMA call enqueues at most
+ * three kernels (operand packing, then the product) plus a memset of the
+ * stream-K flags; a 3xTF32 call enqueues two split passes and the product
+ * per batch entry. No call synchronises the host.
  * Thread safety: calls on different host threads/streams are safe.
  */
 #ifndef DENSE_FP32_MATRIX_07_GB300_SGEMM_H
@@ -45,8 +48,10 @@
 extern "C" {
 #endif
 
-/* Status codes. Every nonzero code returned by sgemm()/sgemm_ex() means that
- * nothing was enqueued on the stream and C is untouched. */
+/* Status codes. A nonzero code returned by a call means that C is untouched:
+ * argument errors return before anything is enqueued; a failing launch may
+ * follow scratch-only work (an operand pack, a TF32 split) already enqueued
+ * on the stream. */
 enum {
     SGEMM_OK = 0,
     SGEMM_ERR_INVALID_VALUE = 1, /* negative size, short leading dimension,
@@ -139,8 +144,10 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K,
  * Pointers are device pointers; C must not overlap A or B (over the whole
  * batch). Transposed operands and rows or batch strides that are not 16-byte
  * multiples are packed into pool scratch first; alpha and beta are applied in
- * the kernels' epilogues; batch entries share one persistent launch (their
- * tiles are one schedule). Status codes as sgemm(); SGEMM_ERR_UNSUPPORTED if
+ * the kernels' epilogues; on the FFMA configurations batch entries share one
+ * persistent launch (their tiles are one schedule), on the 3xTF32 ones each
+ * entry is split and multiplied in turn. Status codes as sgemm();
+ * SGEMM_ERR_UNSUPPORTED if
  * a forced configuration cannot run the general form (the simple and the
  * kernel-ladder configurations run only the plain form).
  */
@@ -244,11 +251,12 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
  * routine, torch's caching allocator included) where they need a product:
  * code whose device memory is fully handed to another allocator or to a
  * fixed-size arena, and latency-critical loops that must not take the
- * driver's allocation path (which can block and synchronise). sgemm() itself
- * allocates only when an operand needs packing (a base address that is not
+ * driver's allocation path (which can block and synchronise). sgemm() takes
+ * pool scratch when an operand needs packing (a base address that is not
  * 16-byte aligned, or a leading dimension that is not a multiple of 4
- * floats); this entry point packs such operands into a fixed scratch array
- * compiled into the library instead, and allocates nothing.
+ * floats) and for the partial sums of a stream-K tail; this entry point packs
+ * such operands into a fixed scratch array compiled into the library instead,
+ * runs whole tiles (no stream-K partial sums), and allocates nothing.
  *
  * Arguments, semantics, ownership and status codes: as sgemm().
  *
