@@ -51,7 +51,9 @@ extern "C" {
 /* Status codes. A nonzero code returned by a call means that C is untouched:
  * argument errors return before anything is enqueued; a failing launch may
  * follow scratch-only work (an operand pack, a TF32 split) already enqueued
- * on the stream. */
+ * on the stream. One exception: in a batched call on a 3xTF32 configuration,
+ * which launches entry after entry, a launch that fails at entry b leaves
+ * entries 0 .. b-1 computed. */
 enum {
     SGEMM_OK = 0,
     SGEMM_ERR_INVALID_VALUE = 1, /* negative size, short leading dimension,
