@@ -17,6 +17,7 @@
 //   5  SGEMM inner loop from shared memory: 8 x 8 thread tiles, 128 x 128
 //      block, A rows 128-byte swizzled (LDS.128 of 4 k), B read as float4
 //   6  as 5 with 8 x 16 thread tiles (128 x 256 block): the main kernel's tile
+//   7  as 5 with 12 warps (3 per SM sub-partition), 192 x 128 block
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -136,16 +137,16 @@ namespace {
 // at chunk c ^ (r & 7); B is [32][BN] floats. Each thread loads 4 k of A per
 // row with one LDS.128 and TN/4 float4 of B per k, then issues TM * TN / 2
 // broadcast FFMA2 per k.
-template <int TN>
-__global__ void __launch_bounds__(256, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
+template <int TN, int WM = 2>
+__global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
 {
     constexpr int TM = 8, TR = 8, TC = 4, WN = 4;
-    constexpr int BM = 128, BN = WN * TC * TN;
+    constexpr int BM = WM * TR * TM, BN = WN * TC * TN, NT = WM * WN * 32;
     extern __shared__ __align__(1024) unsigned char smem[];
     float *sA = reinterpret_cast<float *>(smem);
     float *sB = reinterpret_cast<float *>(smem + BM * 128);
-    for (int e = threadIdx.x; e < BM * 32; e += 256) sA[e] = (e % 7) * 0.25f - 0.5f;
-    for (int e = threadIdx.x; e < BN * 32; e += 256) sB[e] = (e % 5) * 0.125f - 0.25f;
+    for (int e = threadIdx.x; e < BM * 32; e += NT) sA[e] = (e % 7) * 0.25f - 0.5f;
+    for (int e = threadIdx.x; e < BN * 32; e += NT) sB[e] = (e % 5) * 0.125f - 0.25f;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wm = (warp / WN) * TR * TM, wn = (warp % WN) * TC * TN;
@@ -203,18 +204,18 @@ __global__ void __launch_bounds__(256, 1) inner_kernel(float *out, int iters, un
     for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN / 2; ++j) s += acc[i][j].x + acc[i][j].y;
-    out[blockIdx.x * 256 + threadIdx.x] = s;
+    out[blockIdx.x * NT + threadIdx.x] = s;
 }
 
-template <int TN>
-constexpr int inner_smem() { return 128 * 128 + 4 * 4 * TN * 128; }
+template <int TN, int WM = 2>
+constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 
 }  // namespace
 
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 7; }
+int fma_probe_count(void) { return 8; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -227,10 +228,10 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 6 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 7 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
-    if ((e = cudaMalloc(&out, sizeof(float) * 256 * (size_t)sms)) != cudaSuccess) return (int)e;
+    if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
     if ((e = cudaMalloc(&clk, 2 * sizeof(unsigned long long))) != cudaSuccess) {
         cudaFree(out);
         return (int)e;
@@ -245,16 +246,21 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 3: outer_kernel<3><<<sms, 256>>>(out, loop_iters, clk); break;
         case 4: outer_kernel<4><<<sms, 256>>>(out, loop_iters, clk); break;
         case 5: inner_kernel<8><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
-        default: inner_kernel<16><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 6: inner_kernel<16><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        default: inner_kernel<8, 3><<<sms, 384, inner_smem<8, 3>()>>>(out, loop_iters, clk); break;
         }
     };
     if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
     else if (kind <= 4) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind == 5) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind == 6) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<8, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<8, 3>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
     if (e == cudaSuccess) e = cudaEventCreate(&e1);
