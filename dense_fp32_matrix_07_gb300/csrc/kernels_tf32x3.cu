@@ -332,7 +332,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                     const int col0 = col_base + c0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) f[j] *= alpha;
-                    if (VEC_C && col0 + 32 <= N) {
+                    if (VEC_C && (int64_t)col0 + 32 <= N) {   // 64-bit: col0 + 32 may reach 2^31
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);

@@ -133,7 +133,7 @@ __device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_t t, int 
 // slabs on `slots` resident CTAs. Policy (SchedPolicy): whole tiles; forced
 // stream-K over every tile, split down to one slab per CTA (for tests);
 // automatic: stream-K only when whole tiles would leave the last wave below
-// 97 % full and a tile spans at least 8 slabs, keeping at least 4 slabs per
+// 90 % full and a tile spans at least 8 slabs, keeping at least 4 slabs per
 // CTA; or tail split: whole tiles for every full wave, then each leftover
 // tile cut into floor(slots / leftover) >= 2 equal K parts. `with_sk` false
 // always gives whole tiles. Pointers are left null.
