@@ -36,6 +36,10 @@
  * three kernels (operand packing, then the product) plus a memset of the
  * stream-K flags; a 3xTF32 call enqueues two split passes and the product
  * per batch entry. No call synchronises the host.
+ * Graph capture: sgemm(), sgemm_ex(), sgemm_general() and sgemm_general_ex()
+ * may be captured into a CUDA graph once one call has run on the device
+ * (the first call sets the device up); a replay computes the product of
+ * whatever the operand buffers hold at replay time.
  * Thread safety: calls on different host threads/streams are safe.
  */
 #ifndef DENSE_FP32_MATRIX_07_GB300_SGEMM_H
