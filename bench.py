@@ -422,6 +422,8 @@ def main():
     ap.add_argument("--alpha", type=float, default=1.0, help="general form: alpha")
     ap.add_argument("--beta", type=float, default=0.0, help="general form: beta (C is read when nonzero)")
     ap.add_argument("--batch", type=int, default=1, help="general form: strided batch of this many products")
+    ap.add_argument("--noalloc", action="store_true",
+                    help="time the allocation-free entry point sgemm_noalloc instead of sgemm_ex")
     ap.add_argument("--probe-fma", action="store_true",
                     help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
     args = ap.parse_args()
@@ -455,9 +457,11 @@ def main():
     sh = stream.cuda_stream
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     general = args.op_a or args.op_b or args.alpha != 1.0 or args.beta != 0.0 or args.batch > 1
-    if general:
-        # The host-buffer, tensor-core and CPU legs belong to the plain workload.
+    if general or args.noalloc:
+        # The host-buffer, tensor-core and CPU legs belong to the plain sgemm() workload.
         args.no_e2e = args.no_tf32x3 = args.no_cpu_baseline = True
+    if general and args.noalloc:
+        raise SystemExit("--noalloc times the plain form only")
     if not general:
         dA, dB = A.to(dev), B.to(dev)
         dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
@@ -468,8 +472,12 @@ def main():
         flops = product_flops(w.M, w.N, w.K)
 
         def step():
-            r = sg.sgemm_ex(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
-                            dC.data_ptr(), w.ldc, args.config, sh)
+            if args.noalloc:
+                r = sg.sgemm_noalloc(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
+                                     dC.data_ptr(), w.ldc, sh)
+            else:
+                r = sg.sgemm_ex(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb,
+                                dC.data_ptr(), w.ldc, args.config, sh)
             if r != 0:
                 raise RuntimeError(sg.sgemm_error_string(r))
     else:
@@ -717,7 +725,8 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": workload_config(w, cfg_name) if not general else dict(
+        "config": dict(workload_config(w, cfg_name), entry="sgemm_noalloc") if args.noalloc else
+                  workload_config(w, cfg_name) if not general else dict(
             workload_config(w, cfg_name, l2=(f"A+B+C = {total_bytes / 1e6:.1f} MB"
                                              + (": L2 flushed between steps" if flush is not None else " > L2, no flush"))),
             form={"op_a": args.op_a, "op_b": args.op_b, "alpha": args.alpha, "beta": args.beta,

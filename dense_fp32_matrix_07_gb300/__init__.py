@@ -109,9 +109,9 @@ def sgemm_ex(M, N, K, A, lda, B, ldb, C, ldc, config, stream=0) -> int:
 def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """sgemm() for callers that cannot allocate: misaligned operands are
     packed into the library's fixed 64 MiB scratch array instead of
-    allocated scratch; returns SGEMM_ERR_SCRATCH_LIMIT if they would not
-    fit. All calls on a device share that array, so calls that overlap on
-    the GPU race on it."""
+    allocated scratch (SGEMM_ERR_SCRATCH_LIMIT if they would not fit), and
+    stream-K partial sums go in a fixed 24 MiB array. All calls on a device
+    share those arrays, so calls that overlap on the GPU race on them."""
     return load().sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 

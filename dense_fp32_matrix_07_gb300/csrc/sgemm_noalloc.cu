@@ -13,10 +13,15 @@
 // them; later calls on the device reuse the cache. Make that first call
 // before any stream capture begins.
 //
-// Sharing: every call on a device uses the same array, which keeps whatever
-// the last call packed into it. Nothing in it has to start at zero (each call
-// rewrites every packed entry the product reads; the padding at the end of
-// packed rows is never read). Calls whose work overlaps on the GPU (different
+// A second fixed array, 24 MiB, holds the stream-K partial sums and flags of
+// the product's schedule (at most one 128 x 256 tile per SM: about 19 MiB on
+// 152 SMs); a schedule that would need more runs whole tiles instead.
+//
+// Sharing: every call on a device uses the same arrays, which keep whatever
+// the last call left in them. Nothing in it has to start at zero (each call
+// rewrites every packed entry the product reads, the padding at the end of
+// packed rows is never read, and the stream-K flags are zeroed by a memset on
+// the call's stream before its product). Calls whose work overlaps on the GPU (different
 // streams, or different host threads) race on the array and must be ordered
 // by the caller.
 #include "../../include/sgemm.h"
@@ -33,6 +38,12 @@ constexpr int64_t kNoAllocScratchFloats = int64_t(16) << 20;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
+// 24 MiB for the stream-K partial sums and flags: one 128 x 256 FP32 tile
+// (128 KiB) per CTA slot for up to 190 SMs, with room for the flags.
+constexpr size_t kNoAllocWorkspaceBytes = size_t(24) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -42,6 +53,7 @@ struct NoAllocDevice {
     int num_sms = 0;
     unsigned int *status = nullptr;   // device error word
     float *scratch = nullptr;         // device address of g_noalloc_scratch
+    unsigned char *workspace = nullptr;   // device address of g_noalloc_workspace
 };
 
 std::mutex g_na_mutex;
@@ -59,17 +71,19 @@ int noalloc_device(NoAllocDevice **out)
     if (!d.ready) {
         int sms = 0;
         unsigned int *status = nullptr;
-        void *scratch = nullptr;
+        void *scratch = nullptr, *workspace = nullptr;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             sms <= 0 || device_status_word(&status) != cudaSuccess ||
             configs_prepare_device() != cudaSuccess ||
-            cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) {
+            cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch ||
+            cudaGetSymbolAddress(&workspace, g_noalloc_workspace) != cudaSuccess || !workspace) {
             cudaGetLastError();
             return SGEMM_ERR_CUDA;
         }
         d.num_sms = sms;
         d.status = status;
         d.scratch = static_cast<float *>(scratch);
+        d.workspace = static_cast<unsigned char *>(workspace);
         d.ready = true;
     }
     *out = &d;
@@ -162,7 +176,17 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         return SGEMM_ERR_SCRATCH_LIMIT;
 
     GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
-    g.sched = kSchedDataParallel;   // whole tiles: no stream-K workspace needed
+    // The stream-K partial sums and flags go in the fixed workspace array
+    // when they fit (they always do on GPUs of up to 190 SMs); otherwise the
+    // product runs whole tiles, which need no workspace.
+    g.sched = kSchedAuto;
+    const size_t ws_bytes = config_workspace_bytes(cfg, g);
+    if (ws_bytes > 0 && ws_bytes <= kNoAllocWorkspaceBytes) {
+        g.workspace = dev->workspace;
+        g.workspace_bytes = ws_bytes;
+    } else {
+        g.sched = kSchedDataParallel;
+    }
     if (pack_a) {
         if (pack_into_scratch(A, M, K, lda, 0, lda_p, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         g.A = dev->scratch;

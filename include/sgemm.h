@@ -262,7 +262,9 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
  * 16-byte aligned, or a leading dimension that is not a multiple of 4
  * floats) and for the partial sums of a stream-K tail; this entry point packs
  * such operands into a fixed scratch array compiled into the library instead,
- * runs whole tiles (no stream-K partial sums), and allocates nothing.
+ * keeps the stream-K partial sums and flags in a second fixed array (24 MiB;
+ * a schedule needing more, on GPUs of over 190 SMs, runs whole tiles), and
+ * allocates nothing.
  *
  * Arguments, semantics, ownership and status codes: as sgemm().
  *
@@ -271,14 +273,14 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
  * for a packed B. Larger requests return SGEMM_ERR_SCRATCH_LIMIT with nothing
  * enqueued. Aligned operands are not packed and have no size limit.
  *
- * Memory: every GPU that loads the library's device code holds the 64 MiB
- * array until the process exits.
+ * Memory: every GPU that loads the library's device code holds the two
+ * arrays (64 MiB + 24 MiB) until the process exits.
  * Set-up: the first call on a device (with that device current) looks up the
- * array's device address and caches it with the device's other constants;
- * make that first call before any stream capture begins.
- * Sharing: all calls on a device share the one array, which keeps the last
- * call's packed data; calls whose work overlaps on the GPU (other streams,
- * other host threads) race on it, so the caller must order them.
+ * arrays' device addresses and caches them with the device's other
+ * constants; make that first call before any stream capture begins.
+ * Sharing: all calls on a device share the arrays, which keep the last call's
+ * packed data and partial sums; calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on them, so the caller must order them.
  */
 int sgemm_noalloc(int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda,
