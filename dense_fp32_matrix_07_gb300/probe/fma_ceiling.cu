@@ -18,6 +18,8 @@
 //      block, A rows 128-byte swizzled (LDS.128 of 4 k), B read as float4
 //   6  as 5 with 8 x 16 thread tiles (128 x 256 block): the main kernel's tile
 //   7  as 5 with 12 warps (3 per SM sub-partition), 192 x 128 block
+//   8  as 3 with the multiplicands swapped: ffma2(b pair, broadcast a, acc)
+//   9  as 6 with the multiplicands swapped
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(256) peak_kernel(float *out, int iters, float 
 }
 
 // 2 / 3 / 4: 8 x 8 outer products from registers, 32 k per iteration.
-template <int MODE>
+template <int MODE, bool SWAP = false>
 __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, unsigned long long *clk)
 {
     float a[8], bs[8];
@@ -105,7 +107,9 @@ __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, un
                     for (int j = 0; j < 8; ++j) accs[i][j] = fmaf(a[i], bs[j], accs[i][j]);
                 } else if (MODE == 3) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+                    for (int q = 0; q < 4; ++q)
+                        acc[i][q] = SWAP ? __ffma2_rn(b[q], make_float2(a[i], a[i]), acc[i][q])
+                                         : __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
                 } else {
                     const float av = a[(i + k) & 7];
 #pragma unroll
@@ -137,7 +141,7 @@ namespace {
 // at chunk c ^ (r & 7); B is [32][BN] floats. Each thread loads 4 k of A per
 // row with one LDS.128 and TN/4 float4 of B per k, then issues TM * TN / 2
 // broadcast FFMA2 per k.
-template <int TN, int WM = 2>
+template <int TN, int WM = 2, bool SWAP = false>
 __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
 {
     constexpr int TM = 8, TR = 8, TC = 4, WN = 4;
@@ -191,8 +195,13 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
                     const float2 aa = make_float2(a[i][kk], a[i][kk]);
 #pragma unroll
                     for (int g = 0; g < TN / 4; ++g) {
-                        acc[i][2 * g] = __ffma2_rn(aa, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
-                        acc[i][2 * g + 1] = __ffma2_rn(aa, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+                        if (SWAP) {
+                            acc[i][2 * g] = __ffma2_rn(make_float2(b[g].x, b[g].y), aa, acc[i][2 * g]);
+                            acc[i][2 * g + 1] = __ffma2_rn(make_float2(b[g].z, b[g].w), aa, acc[i][2 * g + 1]);
+                        } else {
+                            acc[i][2 * g] = __ffma2_rn(aa, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
+                            acc[i][2 * g + 1] = __ffma2_rn(aa, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+                        }
                     }
                 }
             }
@@ -215,7 +224,7 @@ constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 8; }
+int fma_probe_count(void) { return 10; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -228,7 +237,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 7 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 9 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -247,13 +256,15 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 4: outer_kernel<4><<<sms, 256>>>(out, loop_iters, clk); break;
         case 5: inner_kernel<8><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
         case 6: inner_kernel<16><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
-        default: inner_kernel<8, 3><<<sms, 384, inner_smem<8, 3>()>>>(out, loop_iters, clk); break;
+        case 7: inner_kernel<8, 3><<<sms, 384, inner_smem<8, 3>()>>>(out, loop_iters, clk); break;
+        case 8: outer_kernel<3, true><<<sms, 256>>>(out, loop_iters, clk); break;
+        default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
     if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
-    else if (kind <= 4) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
+    else if (kind <= 4 || kind == 8) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind == 5) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else if (kind == 6) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind == 6 || kind == 9) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
@@ -261,6 +272,9 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kernel<8, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<8, 3>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
     if (e == cudaSuccess) e = cudaEventCreate(&e1);
