@@ -259,6 +259,15 @@ def dist_setup():
     return world, rank, local
 
 
+def host_cores() -> int:
+    """CPU cores this process may run on (a launcher's OMP_NUM_THREADS=1 does
+    not limit the oracle: the timing runs alone on rank 0)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
 def run_reference(args, world, rank):
     """The reference arm: the FP64 CPU oracle over bounded samples of rows."""
     if rank != 0:
@@ -267,6 +276,7 @@ def run_reference(args, world, rank):
     import oracle
     w = workloads.WORKLOADS[args.workload]
     oracle.build()
+    oracle.set_num_threads(args.cpu_threads if args.cpu_threads > 0 else host_cores())
     A, B = workloads.make_workload(w)
     An, Bn = A.numpy(), B.numpy()
     # Size the steps so the whole run (warm-up + timed) takes about 90 s of
@@ -326,8 +336,7 @@ def cpu_baseline(w, A, B, threads=0, budget_s=30.0, min_s=10.0):
     import numpy as np
     import oracle
     oracle.build()
-    if threads > 0:
-        oracle.set_num_threads(threads)
+    oracle.set_num_threads(threads if threads > 0 else host_cores())
     An, Bn = A.numpy(), B.numpy()
     probe = np.arange(min(w.M, oracle.num_threads()), dtype=np.int64)
     t0 = time.perf_counter()
