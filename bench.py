@@ -410,6 +410,27 @@ def run_fma_probe():
     return 0
 
 
+def run_l2_probe(mib):
+    """Every SM reads the same `mib` MiB buffer at once (probe/fma_ceiling.cu,
+    l2_probe_shared_read): under ncu, a cold launch's DRAM bytes against the
+    buffer's size show how often the L2 fetches data all SMs share."""
+    import ctypes
+    from dense_fp32_matrix_07_gb300 import build as _b
+    _b.build()
+    lib = ctypes.CDLL(_b.PROBE_LIB)
+    lib.l2_probe_shared_read.restype = ctypes.c_int
+    lib.l2_probe_shared_read.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    ms = ctypes.c_double()
+    rc = lib.l2_probe_shared_read(int(mib), 5, ctypes.byref(ms))
+    if rc != 0:
+        raise RuntimeError(f"l2 probe: CUDA error {rc}")
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    print(json.dumps({"probe": "l2_shared_read", "mib": mib, "sms": sms, "best_ms": round(ms.value, 4),
+                      "l2_to_sm_gbs": round(sms * mib * 2 ** 20 / (ms.value * 1e-3) / 1e9, 1)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -436,6 +457,8 @@ def main():
                     help="time the allocation-free entry point sgemm_noalloc instead of sgemm_ex")
     ap.add_argument("--probe-fma", action="store_true",
                     help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
+    ap.add_argument("--probe-l2", type=int, default=0, metavar="MIB",
+                    help="every SM reads the same MIB-MiB buffer (L2 sharing probe, for ncu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -445,6 +468,8 @@ def main():
         return run_reference(args, world, rank)
     if args.probe_fma:
         return run_fma_probe()
+    if args.probe_l2:
+        return run_l2_probe(args.probe_l2)
 
     import torch
     import dense_fp32_matrix_07_gb300 as sg

@@ -307,3 +307,76 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
 }
 
 }  // extern "C"
+
+// L2 sharing probe: every block reads the whole of one `n4`-float4 buffer
+// (all blocks at about the same time) and writes one sum. The DRAM bytes of
+// a cold launch, against the buffer's size, show how many times the L2
+// fetches data that every SM reads.
+namespace {
+
+__global__ void __launch_bounds__(1024) l2_shared_read_kernel(const float4 *__restrict__ buf, int64_t n4,
+                                                              float *__restrict__ out)
+{
+    float s = 0.0f;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = buf[i];
+        s += v.x + v.y + v.z + v.w;
+    }
+    __shared__ float red[32];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        out[blockIdx.x] = t;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+// One block of 1024 threads per SM reads the same `mib` MiB buffer; runs
+// `reps` launches (the buffer is written once, before them) and returns the
+// best launch time. Returns 0 or a cudaError_t value.
+int l2_probe_shared_read(int mib, int reps, double *best_ms)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    if (mib < 1 || mib > 4096 || reps < 1) return (int)cudaErrorInvalidValue;
+    const int64_t n4 = (int64_t)mib * (1 << 20) / 16;
+    float4 *buf = nullptr;
+    float *out = nullptr;
+    if ((e = cudaMalloc(&buf, (size_t)n4 * 16)) != cudaSuccess) return (int)e;
+    if ((e = cudaMalloc(&out, sizeof(float) * (size_t)sms)) != cudaSuccess) {
+        cudaFree(buf);
+        return (int)e;
+    }
+    e = cudaMemset(buf, 0, (size_t)n4 * 16);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    float best = 0.0f;
+    for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+        cudaEventRecord(e0);
+        l2_shared_read_kernel<<<sms, 1024>>>(buf, n4, out);
+        cudaEventRecord(e1);
+        e = cudaEventSynchronize(e1);
+        float t = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+        if (r == 0 || t < best) best = t;
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaFree(buf);
+    cudaFree(out);
+    if (e != cudaSuccess) return (int)e;
+    *best_ms = best;
+    return 0;
+}
+
+}  // extern "C"
