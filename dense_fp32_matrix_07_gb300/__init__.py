@@ -31,8 +31,8 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
-            "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_general",
-            "sgemm_general_ex")
+            "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_test_schedule",
+            "sgemm_general", "sgemm_general_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +64,9 @@ def load(rebuild: bool = False):
             lib.sgemm_test_withhold_copy.restype = ctypes.c_int
             lib.sgemm_test_withhold_copy.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
                                                      _i64, ctypes.c_int, _vp]
+            lib.sgemm_test_schedule.restype = ctypes.c_int
+            lib.sgemm_test_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64,
+                                                ctypes.c_int, _i64, _vp, _i64, _vp, _vp]
             lib.sgemm_test_launch_without_cluster.restype = ctypes.c_int
             lib.sgemm_test_launch_without_cluster.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                                               _vp, _i64, _vp]
@@ -127,6 +130,28 @@ def sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream=0)
     kernel launched without its 2-CTA cluster; the kernel detects it, does
     nothing, and sgemm_check_status() reports SGEMM_ERR_LAUNCH."""
     return load().sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def sgemm_test_schedule(M, N, K, bm, bn, bk, slots, policy, batch=1):
+    """Test hook (host only): the persistent kernels' work schedule. Returns
+    (items, info): items an (n, 8) int64 array of CTA, tile, first slab, end
+    slab, batch entry, tile row, tile column, partner end (-1 unless the CTA
+    owns a split tile); info a dict of grid, tiles, dp_tiles, sk_ctas, nk,
+    tiles_m, tiles_n."""
+    import numpy as np
+    count = ctypes.c_int64(0)
+    info = np.zeros(7, dtype=np.int64)
+    cap = 1024
+    while True:
+        items = np.zeros((cap, 8), dtype=np.int64)
+        rc = load().sgemm_test_schedule(M, N, K, bm, bn, bk, slots, policy, batch,
+                                        items.ctypes.data, cap, ctypes.addressof(count), info.ctypes.data)
+        if rc == SGEMM_OK:
+            keys = ("grid", "tiles", "dp_tiles", "sk_ctas", "nk", "tiles_m", "tiles_n")
+            return items[: count.value], dict(zip(keys, (int(x) for x in info)))
+        if count.value <= cap:
+            raise SgemmError(rc, "sgemm_test_schedule")
+        cap = int(count.value)
 
 
 def sgemm_general(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,

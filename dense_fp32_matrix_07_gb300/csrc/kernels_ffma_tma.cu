@@ -296,8 +296,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         if (item.kb1 < sched.nk) {
             // This CTA owns the tile: add the later CTAs' partial sums in order.
-            const int64_t tile_end = (item.tile - sched.dp_tiles + 1) * sched.nk;
-            for (int h = g + 1; h < sched.sk_ctas && sk_start(sched, h) < tile_end; ++h) {
+            const int64_t tile_end = sk_tile_end(sched, item.tile);
+            for (int h = g + 1; sk_holds_part(sched, h, tile_end); ++h) {
                 if (!__all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)h * Cfg::CONSUMERS + warp))) {
                     if (lane == 0) atomicOr(status, kStatusTimeout);
                     return;

@@ -280,8 +280,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
             const bool owner = item.kb0 == 0 && item.kb1 < nk;  // adds later CTAs' partials
             int h_end = g + 1;
             if (owner) {
-                const int64_t tile_end = (item.tile - sched.dp_tiles + 1) * nk;
-                while (h_end < sched.sk_ctas && sk_start(sched, h_end) < tile_end) ++h_end;
+                h_end = sk_partner_end(sched, g, item.tile);
                 bool ok = true;
                 for (int h = g + 1; h < h_end && ok; ++h)
                     ok = __all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)(h * CM + rank) * 4 + q)) != 0;

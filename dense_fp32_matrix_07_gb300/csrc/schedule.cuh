@@ -65,12 +65,37 @@ struct Cursor {
     int64_t sk_pos, sk_end; // this CTA's stream-K iteration range
 };
 
-__device__ __forceinline__ int64_t sk_start(const Schedule &s, int g)
+__host__ __device__ __forceinline__ int64_t sk_start(const Schedule &s, int g)
 {
     return s.sk_iters * g / s.sk_ctas;
 }
 
-__device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
+// Stream-K iteration one past the last slab of stream-K tile `tile`.
+__host__ __device__ __forceinline__ int64_t sk_tile_end(const Schedule &s, int64_t tile)
+{
+    return (tile - s.dp_tiles + 1) * s.nk;
+}
+
+// Whether CTA h, above the owner of a stream-K tile ending at iteration
+// `tile_end`, still holds slabs of that tile (its range starts before the
+// end). The owner's partners are g+1, g+2, ... while this holds.
+__host__ __device__ __forceinline__ bool sk_holds_part(const Schedule &s, int h, int64_t tile_end)
+{
+    return h < s.sk_ctas && sk_start(s, h) < tile_end;
+}
+
+// For the owner g of stream-K tile `tile` (the CTA holding its first slab):
+// one past the last CTA whose range holds later slabs of that tile. The
+// owner adds the partial sums of CTAs g+1 .. end-1, in that order.
+__host__ __device__ __forceinline__ int sk_partner_end(const Schedule &s, int g, int64_t tile)
+{
+    const int64_t tile_end = sk_tile_end(s, tile);
+    int h = g + 1;
+    while (sk_holds_part(s, h, tile_end)) ++h;
+    return h;
+}
+
+__host__ __device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
 {
     Cursor c;
     c.dp_next = g;
@@ -83,7 +108,7 @@ __device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
     return c;
 }
 
-__device__ __forceinline__ bool next_item(const Schedule &s, Cursor &c, Item &it)
+__host__ __device__ __forceinline__ bool next_item(const Schedule &s, Cursor &c, Item &it)
 {
     if (c.dp_next < s.dp_tiles) {
         it.tile = c.dp_next;
@@ -106,13 +131,13 @@ __device__ __forceinline__ bool next_item(const Schedule &s, Cursor &c, Item &it
 
 // Output tile of linear index t: groups of 8 block rows, column-major inside
 // a group, so the CTAs running at the same time touch few A and B panels.
-__device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
+__host__ __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n, int &tm, int &tn)
 {
     constexpr int GR = 8;
     const int64_t per_group = (int64_t)GR * tiles_n;
     const int64_t group = t / per_group;
     const int first_m = (int)(group * GR);
-    const int rows = min(tiles_m - first_m, GR);
+    const int rows = tiles_m - first_m < GR ? tiles_m - first_m : GR;
     const int64_t local = t - group * per_group;
     tm = first_m + (int)(local % rows);
     tn = (int)(local / rows);
@@ -120,7 +145,7 @@ __device__ __forceinline__ void tile_coords(int64_t t, int tiles_m, int tiles_n,
 
 // Batch entry and tile of linear tile index t (batch entries one after the
 // other, the grouped order within each).
-__device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_t t, int &b, int &tm, int &tn)
+__host__ __device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_t t, int &b, int &tm, int &tn)
 {
     const int64_t bb = t / s.tiles_per_batch;
     b = (int)bb;

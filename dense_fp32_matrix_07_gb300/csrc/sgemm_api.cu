@@ -4,6 +4,7 @@
 #include "../../include/sgemm.h"
 #include "common.cuh"
 #include "configs.cuh"
+#include "schedule.cuh"
 
 #include <cstdlib>
 #include <cstring>
@@ -378,6 +379,46 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K, const flo
     Call c{0, 0, M, N, K, 1.0f, A, lda, 0, B, ldb, 0, 0.0f, C, ldc, 0, 1, kCfgTf32x3_pair, -1, -1};
     c.no_cluster = true;
     return sgemm_call(c, stream);
+}
+
+int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
+                        int64_t batch, int64_t *items, int64_t capacity, int64_t *count, int64_t *info)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || bm <= 0 || bn <= 0 || bk <= 0 || slots <= 0 || batch <= 0 ||
+        policy < kSchedAuto || policy > kSchedTailSplit || capacity < 0 || !count || !info)
+        return SGEMM_ERR_INVALID_VALUE;
+    const Schedule s = plan_schedule(M, N, K, bm, bn, bk, slots, policy, true, batch);
+    info[0] = s.grid;
+    info[1] = s.tiles;
+    info[2] = s.dp_tiles;
+    info[3] = s.sk_ctas;
+    info[4] = s.nk;
+    info[5] = s.tiles_m;
+    info[6] = s.tiles_n;
+    int64_t n = 0;
+    for (int g = 0; g < s.grid; ++g) {
+        Cursor cur = cursor_init(s, g);
+        Item it;
+        while (next_item(s, cur, it)) {
+            if (n < capacity) {
+                int b, tm, tn;
+                tile_coords_b(s, it.tile, b, tm, tn);
+                const bool owner = it.kb0 == 0 && it.kb1 < s.nk;
+                int64_t *r = items + 8 * n;
+                r[0] = g;
+                r[1] = it.tile;
+                r[2] = it.kb0;
+                r[3] = it.kb1;
+                r[4] = b;
+                r[5] = tm;
+                r[6] = tn;
+                r[7] = owner ? sk_partner_end(s, g, it.tile) : -1;
+            }
+            ++n;
+        }
+    }
+    *count = n;
+    return n <= capacity ? SGEMM_OK : SGEMM_ERR_INVALID_VALUE;
 }
 
 int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha, const float *A,

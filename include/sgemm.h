@@ -250,6 +250,27 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
                                       float *C, int64_t ldc, cudaStream_t stream);
 
 /*
+ * sgemm_test_schedule — test hook (host only, no GPU): the work schedule the
+ * persistent kernels follow, enumerated.
+ *
+ * Plans the schedule of an M x N x K product (times `batch`) in bm x bn
+ * tiles of bk-deep slabs on `slots` CTAs under `policy` (0 automatic, 1 whole
+ * tiles, 2 stream-K everywhere, 3 tail split), with the stream-K workspace
+ * available, and walks every CTA's work items in the order the kernels do.
+ * Item n fills items[8n .. 8n+7]: CTA, tile, first slab, end slab, batch
+ * entry, tile row, tile column, and, for the owner of a tile split among
+ * several CTAs (it holds the first slab), one past the last CTA whose
+ * partial sums it adds (else -1). info[0..6] receive the grid, tiles, whole
+ * tiles, stream-K CTAs, slabs per tile, tile rows and tile columns.
+ * *count receives the number of items; SGEMM_ERR_INVALID_VALUE if it exceeds
+ * `capacity` (items then holds the first `capacity`) or an argument is out
+ * of range.
+ */
+int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
+                        int64_t slots, int policy, int64_t batch,
+                        int64_t *items, int64_t capacity, int64_t *count, int64_t *info);
+
+/*
  * sgemm_noalloc — sgemm() for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for users of
