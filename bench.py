@@ -379,7 +379,8 @@ def cpu_baseline(w, A, B, threads=0, budget_s=30.0, min_s=10.0):
 FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_registers",
               "ffma2_outer_8x8_registers_fixed", "ffma2_outer_8x8_registers_rotating",
               "sgemm_inner_loop_8x8_smem", "sgemm_inner_loop_8x16_smem", "sgemm_inner_loop_8x8_smem_12warps",
-              "ffma2_outer_8x8_registers_fixed_swapped", "sgemm_inner_loop_8x16_smem_swapped")
+              "ffma2_outer_8x8_registers_fixed_swapped", "sgemm_inner_loop_8x16_smem_swapped",
+              "ffma2_outer_8x8_true_pairs_b_reused", "ffma2_outer_8x8_true_pairs_a_reused")
 
 
 def run_fma_probe():

@@ -20,6 +20,9 @@
 //   7  as 5 with 12 warps (3 per SM sub-partition), 192 x 128 block
 //   8  as 3 with the multiplicands swapped: ffma2(b pair, broadcast a, acc)
 //   9  as 6 with the multiplicands swapped
+//  10  8 x 8 outer product from registers with a held as true pairs (a, a)
+//      (not a broadcast), b pairs reused across the inner loop (b outer)
+//  11  as 10 with a pairs reused across the inner loop (a outer)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -73,7 +76,7 @@ __global__ void __launch_bounds__(256) peak_kernel(float *out, int iters, float 
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
-// 2 / 3 / 4: 8 x 8 outer products from registers, 32 k per iteration.
+// 2 / 3 / 4 / 10 / 11: 8 x 8 outer products from registers, 32 k per iteration.
 template <int MODE, bool SWAP = false>
 __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, unsigned long long *clk)
 {
@@ -86,6 +89,14 @@ __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, un
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) b[q] = make_float2(q * 0.5f, q * 0.25f + threadIdx.x * 1e-4f);
+    // True pairs (a, a + z) with an opaque zero z: the compiler cannot fold
+    // them back into a broadcast of one register.
+    unsigned zbits;
+    asm volatile("mov.u32 %0, 0;" : "=r"(zbits));
+    const float z = __uint_as_float(zbits);
+    float2 a2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a2[i] = make_float2(a[i], a[i] + z);
     float2 acc[8][4];
     float accs[8][8];
 #pragma unroll
@@ -100,6 +111,20 @@ __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, un
     for (int it = 0; it < iters; ++it) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
+            if (MODE == 10) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i][q] = __ffma2_rn(a2[i], b[q], acc[i][q]);
+                continue;
+            }
+            if (MODE == 11) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(a2[i], b[q], acc[i][q]);
+                continue;
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 if (MODE == 2) {
@@ -224,7 +249,7 @@ constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 10; }
+int fma_probe_count(void) { return 12; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -237,7 +262,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 9 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 11 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -258,11 +283,13 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 6: inner_kernel<16><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 7: inner_kernel<8, 3><<<sms, 384, inner_smem<8, 3>()>>>(out, loop_iters, clk); break;
         case 8: outer_kernel<3, true><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 10: outer_kernel<10><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 11: outer_kernel<11><<<sms, 256>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
     if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
-    else if (kind <= 4 || kind == 8) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
+    else if (kind <= 4 || kind == 8 || kind >= 10) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind == 5) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
     else if (kind == 6 || kind == 9) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
