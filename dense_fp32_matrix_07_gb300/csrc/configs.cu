@@ -44,11 +44,13 @@ bool config_supports(int cfg, const ProblemShape &p)
 int select_config(const ProblemShape &p)
 {
     if (!config_supports(kCfgFfma2_128x128, p)) return kCfgTiledSimple;
-    // Tiny products (up to about 320^3, short K) finish sooner in the simple
-    // tiled kernel: no tensor-map set-up, and its 16 x 16 tiles spread over
-    // many SMs (measured at 256^3: 10.3 us against 15.6 us for 128 x 64 TMA
-    // tiles; at 384^3 the TMA kernel is ahead, 17.1 us against 22.5 us).
-    if ((double)p.M * (double)p.N * (double)p.K <= 33554432.0 && p.K <= 1024) return kCfgTiledSimple;
+    // Tiny products (up to about 400^3, short K) finish sooner in the pages'
+    // register-tiled kernel (2 x 2 outputs per thread, padded 32 x 32 shared
+    // tiles): no tensor-map set-up, and its small tiles spread over many SMs.
+    // Measured back to back: 256^3 10.3 us (the simple 16 x 16 kernel the
+    // same, 128 x 64 TMA tiles 15.9 us), 320^3 12.4 us (14.6, 18.5), 384^3
+    // 16.4 us (22.5, 17.0); at 512^3 the TMA kernel leads, 18.5 us.
+    if ((double)p.M * (double)p.N * (double)p.K <= 67108864.0 && p.K <= 1024) return kCfgLadderRegisterTiled2x2;
     // The widest thread tile (8x16) when there are enough 128x256 tiles to
     // give every SM one; 128x128 down to a third of that (at 1024^3, 64
     // tiles: 49.2 us against 51.2 us for 128x64), 128x64 (two CTAs per SM)

@@ -253,8 +253,8 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
 
     const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, dev->num_sms};
     int cfg = c.config < 0 ? select_config(p) : c.config;
-    // The automatic choice for tiny products is the plain-form-only tiled
-    // kernel; the general form takes the smallest TMA tiles instead.
+    // The automatic choice for tiny products is a plain-form-only kernel of
+    // the pages' ladder; the general form takes the smallest TMA tiles instead.
     if (c.config < 0 && !plain && !kConfigTable[cfg].uses_tma) cfg = kCfgFfma2_128x64;
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
     // Kernels without TMA (the simple and ladder kernels) run the plain form only.

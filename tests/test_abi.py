@@ -84,14 +84,16 @@ def test_plan_packs_only_misaligned_operands():
     assert rc == 0 and (pa, pb) == (1, 0)
     rc, cfg, pa, pb = sg.sgemm_plan(1024, 1024, 1024, 1024, 1024, 1024, 0, 8, 12, 148)
     assert rc == 0 and (pa, pb) == (0, 1)
-    # The simple tiled kernel (tiny products) reads any layout in place.
+    # The register-tiled kernel of the pages' ladder (tiny products) reads any
+    # layout in place.
     rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 4, 8, 12, 148)
-    assert rc == 0 and sg.sgemm_config_name(cfg) == "tiled16_simple" and (pa, pb) == (0, 0)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == "ladder_register_tiled_2x2" and (pa, pb) == (0, 0)
 
 
 @pytest.mark.parametrize("n,name", [
-    (256, "tiled16_simple"),            # tiny: no TMA set-up
-    (384, "ffma2_128x64_k32_s4"),       # 9 tiles of 128x128: the smallest TMA tiles
+    (256, "ladder_register_tiled_2x2"), # tiny: no TMA set-up, small tiles over many SMs
+    (384, "ladder_register_tiled_2x2"),
+    (512, "ffma2_128x64_k32_s4"),       # 16 tiles of 128x128: the smallest TMA tiles
     (1024, "ffma2_128x128_k32_s4"),     # 64 tiles of 128x128 (>= a third of the SMs)
     (2048, "ffma2_128x128_k32_s4"),     # 128 tiles of 128x256 < 148 SMs
     (4096, "ffma2_128x256_k32_s4"),     # 512 tiles of 128x256
@@ -102,7 +104,7 @@ def test_plan_tile_size_follows_the_problem(n, name):
 
 
 def test_plan_long_k_skips_the_simple_kernel():
-    # A tiny output with a long K goes to the stream-K kernel, not one 16x16 block.
+    # A tiny output with a long K goes to the stream-K kernel, not one small block.
     rc, cfg, *_ = sg.sgemm_plan(1, 1, 1 << 20, 1 << 20, 1, 1, 0, 0, 0, 148)
     assert rc == 0 and sg.sgemm_config_name(cfg).startswith("ffma")
 
