@@ -380,7 +380,12 @@ FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_reg
               "ffma2_outer_8x8_registers_fixed", "ffma2_outer_8x8_registers_rotating",
               "sgemm_inner_loop_8x8_smem", "sgemm_inner_loop_8x16_smem", "sgemm_inner_loop_8x8_smem_12warps",
               "ffma2_outer_8x8_registers_fixed_swapped", "sgemm_inner_loop_8x16_smem_swapped",
-              "ffma2_outer_8x8_true_pairs_b_reused", "ffma2_outer_8x8_true_pairs_a_reused")
+              "ffma2_outer_8x8_true_pairs_b_reused", "ffma2_outer_8x8_true_pairs_a_reused",
+              "ffma2_outer_8x8_registers_row_serpentine", "ffma2_outer_8x8_registers_column_serpentine",
+              "ffma2_outer_8x16_registers", "ffma2_outer_8x16_registers_row_serpentine",
+              "ffma2_outer_8x16_registers_column_serpentine",
+              "sgemm_inner_loop_8x16_smem_row_serpentine", "sgemm_inner_loop_8x16_smem_column_serpentine",
+              "sgemm_inner_loop_8x8_smem_row_serpentine", "sgemm_inner_loop_8x8_smem_column_serpentine")
 
 
 def run_fma_probe():

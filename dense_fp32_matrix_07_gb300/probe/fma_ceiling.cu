@@ -23,6 +23,19 @@
 //  10  8 x 8 outer product from registers with a held as true pairs (a, a)
 //      (not a broadcast), b pairs reused across the inner loop (b outer)
 //  11  as 10 with a pairs reused across the inner loop (a outer)
+// The order of the FFMA2s of one k step (ORDER below): 0 row-major (for each
+// row i, every b pair q: the row change swaps both multiplicands), 1 row
+// serpentine (q runs backwards on odd rows, so consecutive FFMA2s always
+// share a multiplicand), 2 column serpentine (b pair outer, rows alternate).
+//  12  8 x 8 outer product from registers, broadcast a, row serpentine
+//  13  as 12, column serpentine
+//  14  8 x 16 outer product from registers, broadcast a, row-major
+//  15  as 14, row serpentine
+//  16  as 14, column serpentine
+//  17  as 6 (8 x 16 from shared memory), row serpentine
+//  18  as 6, column serpentine
+//  19  as 5 (8 x 8 from shared memory), row serpentine
+//  20  as 5, column serpentine
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -156,6 +169,61 @@ __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, un
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// One k step of a TM x (2 NP) outer product: acc[i][q] += a[i] * b[q], the
+// scalar a[i] broadcast to both lanes of the FFMA2, in the given ORDER.
+template <int ORDER, int TM, int NP>
+__device__ __forceinline__ void outer_step(float2 (&acc)[TM][NP], const float (&a)[TM], const float2 (&b)[NP])
+{
+    if constexpr (ORDER == 2) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+#pragma unroll
+            for (int ii = 0; ii < TM; ++ii) {
+                const int i = (q & 1) ? TM - 1 - ii : ii;
+                acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+            }
+    } else {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int qq = 0; qq < NP; ++qq) {
+                const int q = (ORDER == 1 && (i & 1)) ? NP - 1 - qq : qq;
+                acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+            }
+    }
+}
+
+// 12 - 16: 8 x (2 NP) outer products from registers in a given order, 32 k
+// per iteration, fixed operand registers.
+template <int NP, int ORDER>
+__global__ void __launch_bounds__(256, 1) ordered_outer_kernel(float *out, int iters, unsigned long long *clk)
+{
+    float a[8];
+    float2 b[NP];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = threadIdx.x * 1e-3f + i;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) b[q] = make_float2(q * 0.5f, q * 0.25f + threadIdx.x * 1e-4f);
+    float2 acc[8][NP];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < NP; ++q) acc[i][q] = make_float2(0.f, 0.f);
+    const long long c0 = clock64();
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) outer_step<ORDER>(acc, a, b);
+    }
+    record(clk, c0, t0);
+    float s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < NP; ++q) s += acc[i][q].x + acc[i][q].y;
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 }  // namespace
 
 namespace {
@@ -166,7 +234,7 @@ namespace {
 // at chunk c ^ (r & 7); B is [32][BN] floats. Each thread loads 4 k of A per
 // row with one LDS.128 and TN/4 float4 of B per k, then issues TM * TN / 2
 // broadcast FFMA2 per k.
-template <int TN, int WM = 2, bool SWAP = false>
+template <int TN, int WM = 2, bool SWAP = false, int ORDER = -1>
 __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
 {
     constexpr int TM = 8, TR = 8, TC = 4, WN = 4;
@@ -215,6 +283,19 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
 #pragma unroll
                 for (int g = 0; g < TN / 4; ++g)
                     b[g] = *reinterpret_cast<const float4 *>(Bi + k * BN * 4 + g * TC * 16);
+                if constexpr (ORDER >= 0) {
+                    float ak[TM];
+                    float2 b2[TN / 2];
+#pragma unroll
+                    for (int i = 0; i < TM; ++i) ak[i] = a[i][kk];
+#pragma unroll
+                    for (int g = 0; g < TN / 4; ++g) {
+                        b2[2 * g] = make_float2(b[g].x, b[g].y);
+                        b2[2 * g + 1] = make_float2(b[g].z, b[g].w);
+                    }
+                    outer_step<ORDER>(acc, ak, b2);
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < TM; ++i) {
                     const float2 aa = make_float2(a[i][kk], a[i][kk]);
@@ -249,7 +330,7 @@ constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 12; }
+int fma_probe_count(void) { return 21; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -262,7 +343,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 11 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 20 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -285,13 +366,23 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 8: outer_kernel<3, true><<<sms, 256>>>(out, loop_iters, clk); break;
         case 10: outer_kernel<10><<<sms, 256>>>(out, loop_iters, clk); break;
         case 11: outer_kernel<11><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 12: ordered_outer_kernel<4, 1><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 13: ordered_outer_kernel<4, 2><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 14: ordered_outer_kernel<8, 0><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 15: ordered_outer_kernel<8, 1><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 16: ordered_outer_kernel<8, 2><<<sms, 256>>>(out, loop_iters, clk); break;
+        case 17: inner_kernel<16, 2, false, 1><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 18: inner_kernel<16, 2, false, 2><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 19: inner_kernel<8, 2, false, 1><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
+        case 20: inner_kernel<8, 2, false, 2><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
     if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
-    else if (kind <= 4 || kind == 8 || kind >= 10) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
-    else if (kind == 5) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else if (kind == 6 || kind == 9) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind <= 4 || kind == 8 || (kind >= 10 && kind <= 13)) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
+    else if (kind >= 14 && kind <= 16) f = 2.0 * 128 * 32 * (double)loop_iters * 256.0 * sms;
+    else if (kind == 5 || kind >= 19) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
+    else if (kind == 6 || kind == 9 || kind == 17 || kind == 18) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
@@ -301,6 +392,12 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
                                  inner_smem<8, 3>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kernel<16, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
