@@ -385,7 +385,9 @@ FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_reg
               "ffma2_outer_8x16_registers", "ffma2_outer_8x16_registers_row_serpentine",
               "ffma2_outer_8x16_registers_column_serpentine",
               "sgemm_inner_loop_8x16_smem_row_serpentine", "sgemm_inner_loop_8x16_smem_column_serpentine",
-              "sgemm_inner_loop_8x8_smem_row_serpentine", "sgemm_inner_loop_8x8_smem_column_serpentine")
+              "sgemm_inner_loop_8x8_smem_row_serpentine", "sgemm_inner_loop_8x8_smem_column_serpentine",
+              "sgemm_inner_loop_8x16_smem_zigzag_strips", "sgemm_inner_loop_8x16_smem_column_serpentine_halves",
+              "sgemm_inner_loop_8x16_smem_column_serpentine_reversed_odd_k")
 
 
 def run_fma_probe():

@@ -44,10 +44,15 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
         sk = true;
     } else if (with_sk && policy == kSchedAuto) {
         const int64_t rounds = (s.tiles + slots - 1) / slots;
-        // Whole tiles unless the last wave is less than 90 % full (at 1536^3
-        // on 128 x 128 tiles, 144 tiles on 152 SMs, whole tiles measured
-        // 123.1 us against 126.1 us with the stream-K tail).
-        sk = (double)s.tiles < 0.90 * (double)(rounds * slots) && s.nk >= 8;
+        // With at least one full wave ahead of it, a partial last wave is
+        // worth evening out as soon as it idles 0.5 % of the slots (128 x 256
+        // tiles, same-box A/B against whole tiles: 3072^3 0.867 vs 0.903 ms,
+        // 8192^3 16.05 vs 16.66 ms, 12288^3 54.08 vs 55.29 ms; 16384^3, 99.8 %
+        // full, stays whole). A single partial wave, where every tile would
+        // be split, only below 90 % (at 1536^3 on 128 x 128 tiles, 144 tiles
+        // on 152 SMs, whole tiles measured 123.1 us against 126.1 us).
+        const double fill = (double)s.tiles / (double)(rounds * slots);
+        sk = s.nk >= 8 && (rounds >= 2 ? fill < 0.995 : fill < 0.90);
     }
     if (!sk) return s;
     const int64_t full_rounds = s.tiles / slots;

@@ -157,9 +157,10 @@ __host__ __device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_
 // Plans the schedule of an M x N x K product in bm x bn tiles with bk-deep
 // slabs on `slots` resident CTAs. Policy (SchedPolicy): whole tiles; forced
 // stream-K over every tile, split down to one slab per CTA (for tests);
-// automatic: stream-K only when whole tiles would leave the last wave below
-// 90 % full and a tile spans at least 8 slabs, keeping at least 4 slabs per
-// CTA; or tail split: whole tiles for every full wave, then each leftover
+// automatic: stream-K only when a tile spans at least 8 slabs and whole
+// tiles would leave slots idle: more than 0.5 % of them when at least one
+// full wave precedes the last, more than 10 % when all tiles fit in one
+// partial wave; it keeps at least 4 slabs per CTA; or tail split: whole tiles for every full wave, then each leftover
 // tile cut into floor(slots / leftover) >= 2 equal K parts. `with_sk` false
 // always gives whole tiles. Pointers are left null.
 Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,

@@ -36,6 +36,10 @@
 //  18  as 6, column serpentine
 //  19  as 5 (8 x 8 from shared memory), row serpentine
 //  20  as 5, column serpentine
+//  21  as 6, zigzag down strips of two b pairs (each FFMA2 shares a
+//      multiplicand with the one before)
+//  22  as 6, column serpentine over each half of the rows in turn
+//  23  as 6, column serpentine, b pairs in reverse order on odd k
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -172,9 +176,45 @@ __global__ void __launch_bounds__(256, 1) outer_kernel(float *out, int iters, un
 // One k step of a TM x (2 NP) outer product: acc[i][q] += a[i] * b[q], the
 // scalar a[i] broadcast to both lanes of the FFMA2, in the given ORDER.
 template <int ORDER, int TM, int NP>
-__device__ __forceinline__ void outer_step(float2 (&acc)[TM][NP], const float (&a)[TM], const float2 (&b)[NP])
+__device__ __forceinline__ void outer_step(float2 (&acc)[TM][NP], const float (&a)[TM], const float2 (&b)[NP],
+                                           int kk = 0)
 {
-    if constexpr (ORDER == 2) {
+    if constexpr (ORDER == 3) {
+        // zigzag down strips of two b pairs: (i,p) (i,p+1) (i+1,p+1) (i+1,p) ...
+#pragma unroll
+        for (int p0 = 0; p0 < NP; p0 += 2)
+#pragma unroll
+            for (int ii = 0; ii < TM; ++ii) {
+                const int i = (p0 & 2) ? TM - 1 - ii : ii;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int q = p0 + ((ii & 1) ? 1 - e : e);
+                    acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+                }
+            }
+    } else if constexpr (ORDER == 4) {
+        // column serpentine over each half of the rows in turn
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+#pragma unroll
+                for (int ii = 0; ii < TM / 2; ++ii) {
+                    const int i = h * (TM / 2) + ((q & 1) ? TM / 2 - 1 - ii : ii);
+                    acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+                }
+    } else if constexpr (ORDER == 5) {
+        // column serpentine with the b pairs taken in reverse on odd k
+#pragma unroll
+        for (int qq = 0; qq < NP; ++qq) {
+            const int q = (kk & 1) ? NP - 1 - qq : qq;
+#pragma unroll
+            for (int ii = 0; ii < TM; ++ii) {
+                const int i = (qq & 1) ? TM - 1 - ii : ii;
+                acc[i][q] = __ffma2_rn(make_float2(a[i], a[i]), b[q], acc[i][q]);
+            }
+        }
+    } else if constexpr (ORDER == 2) {
 #pragma unroll
         for (int q = 0; q < NP; ++q)
 #pragma unroll
@@ -293,7 +333,7 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
                         b2[2 * g] = make_float2(b[g].x, b[g].y);
                         b2[2 * g + 1] = make_float2(b[g].z, b[g].w);
                     }
-                    outer_step<ORDER>(acc, ak, b2);
+                    outer_step<ORDER>(acc, ak, b2, kk);
                     continue;
                 }
 #pragma unroll
@@ -330,7 +370,7 @@ constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 21; }
+int fma_probe_count(void) { return 24; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -343,7 +383,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 20 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 23 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -375,14 +415,17 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 18: inner_kernel<16, 2, false, 2><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 19: inner_kernel<8, 2, false, 1><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
         case 20: inner_kernel<8, 2, false, 2><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
+        case 21: inner_kernel<16, 2, false, 3><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 22: inner_kernel<16, 2, false, 4><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 23: inner_kernel<16, 2, false, 5><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
     if (kind <= 1) f = 2.0 * 16 * peak_iters * 256.0 * sms;
     else if (kind <= 4 || kind == 8 || (kind >= 10 && kind <= 13)) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind >= 14 && kind <= 16) f = 2.0 * 128 * 32 * (double)loop_iters * 256.0 * sms;
-    else if (kind == 5 || kind >= 19) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else if (kind == 6 || kind == 9 || kind == 17 || kind == 18) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind == 5 || kind == 19 || kind == 20) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
+    else if (kind == 6 || kind == 9 || kind >= 17) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
@@ -398,6 +441,15 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
                                  inner_smem<16>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);

@@ -114,6 +114,11 @@ def test_auto_policy_choices():
     # 16384^3: the last wave is 99.8 % full, so whole tiles only.
     _, info = sg.sgemm_test_schedule(16384, 16384, 16384, 128, 256, 32, 152, AUTO)
     assert info["sk_ctas"] == 0 and info["dp_tiles"] == info["tiles"]
-    # 1536^3 on 128x128 tiles: a 94.7 % last wave stays whole tiles (>= 90 %).
+    # 1536^3 on 128x128 tiles: one wave, 94.7 % full, stays whole tiles (>= 90 %).
     _, info = sg.sgemm_test_schedule(1536, 1536, 1536, 128, 128, 32, 152, AUTO)
     assert info["sk_ctas"] == 0
+    # 8192^3 on 128x256 tiles: 13.47 waves, 96.2 % of the slots busy under
+    # whole tiles; after a full wave that is evened out: 12 whole-tile waves,
+    # then stream-K over the last 200 tiles.
+    _, info = sg.sgemm_test_schedule(8192, 8192, 8192, 128, 256, 32, 152, AUTO)
+    assert info["dp_tiles"] == 12 * 152 and info["sk_ctas"] == 152
