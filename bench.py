@@ -439,6 +439,55 @@ def run_l2_probe(mib):
     return 0
 
 
+def run_shape_sweep(shapes, config):
+    """Times the product on each "MxNxK" shape (tight strides, N(0,1) inputs
+    drawn on the device from seed 0) back to back, with the automatic
+    configuration or the forced one; one JSON line for the whole sweep. For
+    schedule and selector measurements, not a bench line."""
+    import torch
+    import dense_fp32_matrix_07_gb300 as sg
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    peak = sms * FP32_LANES_PER_SM * 2 * measured_sm_max_mhz() * 1e6 / 1e12
+    out = []
+    for shp in shapes:
+        M, N, K = (int(x) for x in shp.lower().split("x"))
+        g = torch.Generator(device=dev).manual_seed(0)
+        A = torch.randn(M, K, device=dev, generator=g)
+        B = torch.randn(K, N, device=dev, generator=g)
+        C = torch.empty(M, N, device=dev)
+        rc, auto_cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(), C.data_ptr(), sms)
+        cfg = config if config >= 0 else auto_cfg
+
+        def call():
+            rc = sg.sgemm_ex(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, cfg, sh)
+            if rc != 0:
+                raise RuntimeError(f"sgemm_ex({shp}, config {cfg}): {sg.sgemm_error_string(rc)}")
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        reps = min(200, max(3, int(3e13 / (2.0 * M * N * K))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rc = sg.sgemm_check_status(sh)
+        if rc != 0:
+            raise RuntimeError(f"{shp}: {sg.sgemm_error_string(rc)}")
+        ms = e0.elapsed_time(e1) / reps
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out.append({"shape": shp, "config": sg.sgemm_config_name(cfg), "reps": reps, "ms": round(ms, 4),
+                    "tflops": round(tf, 2), "fp32_peak_pct": round(100.0 * tf / peak, 2)})
+        del A, B, C
+    print(json.dumps({"sweep": "shapes", "sms": sms, "peak_tflops": round(peak, 3), "results": out}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +514,8 @@ def main():
                     help="time the allocation-free entry point sgemm_noalloc instead of sgemm_ex")
     ap.add_argument("--probe-fma", action="store_true",
                     help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
+    ap.add_argument("--shapes", default="", metavar="MxNxK[,MxNxK...]",
+                    help="time the product on these shapes back to back (automatic or --config) and exit")
     ap.add_argument("--probe-l2", type=int, default=0, metavar="MIB",
                     help="every SM reads the same MIB-MiB buffer (L2 sharing probe, for ncu) and exit")
     args = ap.parse_args()
@@ -478,6 +529,8 @@ def main():
         return run_fma_probe()
     if args.probe_l2:
         return run_l2_probe(args.probe_l2)
+    if args.shapes:
+        return run_shape_sweep([x for x in args.shapes.split(",") if x], args.config)
 
     import torch
     import dense_fp32_matrix_07_gb300 as sg
