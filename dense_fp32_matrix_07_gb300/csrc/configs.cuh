@@ -24,6 +24,7 @@ enum KernelId : int {
     kKernFfma2_128x128k16s8,    // 128x128 block, BK 16, 8 stages, FFMA2
     kKernFfma2_128x64k32s4,     // 128x64 block (4 consumer warps), 2 CTAs per SM
     kKernFfma2_128x256k32s4,    // 128x256 block, 8x16 thread tiles, FFMA2
+    kKernFfma2_128x256k32s4ka,  // the same with A stored K x M (k-major slabs)
     // The pages' kernel ladder (kernels_ladder.cu), for measurement.
     kKernLadderNaive,           // one thread per output, threadIdx.x -> row
     kKernLadderCoalesced,       // one thread per output, threadIdx.x -> column
@@ -58,6 +59,7 @@ enum ConfigId : int {
     kCfgTf32x3_128x256_dp,
     kCfgTf32x3_pair,
     kCfgTf32x3_pair_dp,
+    kCfgFfma2_128x256_ka,
     kNumConfigs
 };
 
@@ -68,6 +70,7 @@ struct ConfigInfo {
     bool uses_tma;   // TMA tensor maps (32-bit coordinates)
     bool packs;      // needs A and B with 16-byte-aligned rows (packs others)
     int bm, bn;      // block tile
+    bool a_kmajor = false;   // takes A stored K x M (transposes a plain A into scratch)
 };
 
 extern const ConfigInfo kConfigTable[kNumConfigs];

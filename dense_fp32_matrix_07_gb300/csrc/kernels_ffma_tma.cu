@@ -55,11 +55,15 @@ namespace sgemm_gb300 {
 
 namespace {
 
-template <int BM_, int BN_, int BK_, int STAGES_, int TN_, bool PAIRED_, int MIN_BLOCKS_>
+template <int BM_, int BN_, int BK_, int STAGES_, int TN_, bool PAIRED_, int MIN_BLOCKS_, bool A_KMAJOR_ = false>
 struct FfmaTmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr bool PAIRED = PAIRED_;   // FFMA2 (two FP32 FMAs per instruction)
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
+    // A stored K x M (k-major: the slab is [BK][BM], M contiguous) instead of
+    // M x K. One LDS.128 then gives a thread 4 of its rows at one k in
+    // consecutive registers.
+    static constexpr bool A_KMAJOR = A_KMAJOR_;
     // Thread tile TM x TN; warp = 8 x 4 threads, so warp tile 64 x 4*TN.
     static constexpr int TM = 8, TN = TN_, G = TN / 4;
     static constexpr int TROWS = 8, TCOLS = 4;
@@ -78,7 +82,7 @@ struct FfmaTmaCfg {
     static constexpr int PRODUCER_REGS = 40;
     static constexpr int CONSUMER_REGS =
         ((LAUNCH_REGS * THREADS - PRODUCER_REGS * 32 * PRODUCER_WARPS) / CONSUMER_THREADS) / 8 * 8;
-    static constexpr int A_ROW_BYTES = BK * 4;
+    static constexpr int A_ROW_BYTES = A_KMAJOR ? BM * 4 : BK * 4;   // one row of the smem slab
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_ROW_BYTES = BN * 4;
     static constexpr int B_BYTES = BK * BN * 4;
@@ -86,13 +90,16 @@ struct FfmaTmaCfg {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGES * 8;
     // Row r of the A slab has its 16-byte chunk c stored at chunk c ^ swz(r),
     // swz(r) = r & 7 for 128-byte rows, (r >> 1) & 3 for 64-byte rows.
+    // A k-major slab is read along its rows without conflicts and needs none.
     static constexpr CUtensorMapSwizzle A_SWIZZLE =
-        BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        A_KMAJOR ? CU_TENSOR_MAP_SWIZZLE_NONE
+                 : (BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     static_assert(TN % 4 == 0 && TN >= 8 && TN <= 16, "thread tile columns: 8, 12 or 16");
     static_assert(BM % WM == 0 && BN % WN == 0, "block tile must hold whole warp tiles");
     static_assert(BK == 32 || BK == 16, "BK is 16 or 32");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage buffers stay 1024-aligned");
     static_assert(BN <= 256 && BM <= 256, "TMA box dimensions are at most 256");
+    static_assert(!A_KMAJOR || (PAIRED && WM == 64), "k-major A: FFMA2 and 64-row warp tiles");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BM * BN == CONSUMER_THREADS * TM * TN, "one partial sum per accumulator");
     static_assert(!REG_SPLIT || (CONSUMERS % 4 == 0 && CONSUMER_REGS <= 255), "whole consumer warpgroups");
@@ -174,8 +181,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                 // issued, so the consumers' wait for it must time out.
                 if (g == 0 && (int)it == withhold_it) continue;
                 ptx::mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
-                ptx::tma_load_3d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), kb * BK, tm * BM, bt * ep.a_bz,
-                                 policy);
+                if constexpr (Cfg::A_KMAJOR)
+                    ptx::tma_load_3d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), tm * BM, kb * BK,
+                                     bt * ep.a_bz, policy);
+                else
+                    ptx::tma_load_3d(sA + s * Cfg::A_BYTES, &mapA, full_bar(s), kb * BK, tm * BM,
+                                     bt * ep.a_bz, policy);
                 ptx::tma_load_3d(sB + s * Cfg::B_BYTES, &mapB, full_bar(s), tn * BN, kb * BK, bt * ep.b_bz,
                                  policy);
                 last_round[s] = round;
@@ -196,7 +207,11 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     const int wn = (warp % Cfg::WARPS_N) * Cfg::WN;
     const int ty = lane / Cfg::TCOLS;   // 0..7: thread row (rows wm + ty + 8i)
     const int tx = lane % Cfg::TCOLS;   // 0..3: thread column (cols wn + 4tx + 16q + e)
-    const uint32_t a_row_off = (uint32_t)(wm + ty) * Cfg::A_ROW_BYTES;
+    // Row-major A slab: this thread's rows wm+ty+8i start at row wm+ty;
+    // k-major slab: its rows are wm+4ty+i and wm+32+4ty+i (i < 4), at byte
+    // (wm+4ty)*4 (and 128 bytes on) of every k row.
+    const uint32_t a_row_off =
+        Cfg::A_KMAJOR ? (uint32_t)(wm + 4 * ty) * 4 : (uint32_t)(wm + ty) * Cfg::A_ROW_BYTES;
     const uint32_t a_xor = (BK == 32) ? (uint32_t)(ty & 7) : (uint32_t)((ty >> 1) & 3);
     const uint32_t b_col_off = (uint32_t)(wn + tx * 4) * 4;
     const int ct = warp * 32 + lane;    // consumer thread index (partial-sum layout)
@@ -228,48 +243,73 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             }
             const uint8_t *As = base_ptr + s * Cfg::A_BYTES + a_row_off;
             const uint8_t *Bs = base_ptr + STAGES * Cfg::A_BYTES + s * Cfg::B_BYTES + b_col_off;
+            if constexpr (Cfg::A_KMAJOR) {
+                // Per k: rows wm+4ty..+3 and wm+32+4ty..+3 as two float4.
 #pragma unroll
-            for (int kg = 0; kg < BK / 4; ++kg) {
-                // A fragment: rows wm+ty+8i, columns 4kg..4kg+3 of the slab.
-                float4 a[8];
-                const uint32_t chunk = ((uint32_t)kg ^ a_xor) << 4;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    a[i] = *reinterpret_cast<const float4 *>(As + i * 8 * Cfg::A_ROW_BYTES + chunk);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int k = kg * 4 + kk;
+                for (int k = 0; k < BK; ++k) {
+                    const float4 lo = *reinterpret_cast<const float4 *>(As + k * Cfg::A_ROW_BYTES);
+                    const float4 hi = *reinterpret_cast<const float4 *>(As + k * Cfg::A_ROW_BYTES + 128);
+                    const float av[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     float4 b[G];
 #pragma unroll
                     for (int q = 0; q < G; ++q)
                         b[q] = *reinterpret_cast<const float4 *>(Bs + k * Cfg::B_ROW_BYTES + 64 * q);
-                    if constexpr (Cfg::PAIRED) {
-                        // Column-serpentine order: each b pair meets the 8
-                        // rows in turn, odd pairs walking the rows upwards, so
-                        // consecutive FFMA2s always share a multiplicand
-                        // register (87.9 % of the FP32 pipe for this loop
-                        // measured alone, against 83.7 % row by row).
+                    // Column-serpentine order, as below.
 #pragma unroll
-                        for (int p = 0; p < TN / 2; ++p) {
-                            const float4 &bq = b[p / 2];
-                            const float2 bp = (p & 1) ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+                    for (int p = 0; p < TN / 2; ++p) {
+                        const float4 &bq = b[p / 2];
+                        const float2 bp = (p & 1) ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
 #pragma unroll
-                            for (int ii = 0; ii < 8; ++ii) {
-                                const int i = (p & 1) ? 7 - ii : ii;
-                                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                                accp[i][p] = __ffma2_rn(make_float2(av, av), bp, accp[i][p]);
-                            }
+                        for (int ii = 0; ii < 8; ++ii) {
+                            const int i = (p & 1) ? 7 - ii : ii;
+                            accp[i][p] = __ffma2_rn(make_float2(av[i], av[i]), bp, accp[i][p]);
                         }
-                    } else {
+                    }
+                }
+            } else {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                for (int kg = 0; kg < BK / 4; ++kg) {
+                    // A fragment: rows wm+ty+8i, columns 4kg..4kg+3 of the slab.
+                    float4 a[8];
+                    const uint32_t chunk = ((uint32_t)kg ^ a_xor) << 4;
 #pragma unroll
-                            for (int q = 0; q < G; ++q) {
-                                acc[i][4 * q + 0] = fmaf(av, b[q].x, acc[i][4 * q + 0]);
-                                acc[i][4 * q + 1] = fmaf(av, b[q].y, acc[i][4 * q + 1]);
-                                acc[i][4 * q + 2] = fmaf(av, b[q].z, acc[i][4 * q + 2]);
-                                acc[i][4 * q + 3] = fmaf(av, b[q].w, acc[i][4 * q + 3]);
+                    for (int i = 0; i < 8; ++i)
+                        a[i] = *reinterpret_cast<const float4 *>(As + i * 8 * Cfg::A_ROW_BYTES + chunk);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k = kg * 4 + kk;
+                        float4 b[G];
+#pragma unroll
+                        for (int q = 0; q < G; ++q)
+                            b[q] = *reinterpret_cast<const float4 *>(Bs + k * Cfg::B_ROW_BYTES + 64 * q);
+                        if constexpr (Cfg::PAIRED) {
+                            // Column-serpentine order: each b pair meets the 8
+                            // rows in turn, odd pairs walking the rows upwards, so
+                            // consecutive FFMA2s always share a multiplicand
+                            // register (87.9 % of the FP32 pipe for this loop
+                            // measured alone, against 83.7 % row by row).
+#pragma unroll
+                            for (int p = 0; p < TN / 2; ++p) {
+                                const float4 &bq = b[p / 2];
+                                const float2 bp = (p & 1) ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+#pragma unroll
+                                for (int ii = 0; ii < 8; ++ii) {
+                                    const int i = (p & 1) ? 7 - ii : ii;
+                                    const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                                    accp[i][p] = __ffma2_rn(make_float2(av, av), bp, accp[i][p]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                                for (int q = 0; q < G; ++q) {
+                                    acc[i][4 * q + 0] = fmaf(av, b[q].x, acc[i][4 * q + 0]);
+                                    acc[i][4 * q + 1] = fmaf(av, b[q].y, acc[i][4 * q + 1]);
+                                    acc[i][4 * q + 2] = fmaf(av, b[q].z, acc[i][4 * q + 2]);
+                                    acc[i][4 * q + 3] = fmaf(av, b[q].w, acc[i][4 * q + 3]);
+                                }
                             }
                         }
                     }
@@ -326,12 +366,13 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
 
-        // Epilogue: rows wm+ty+8i, G runs of 4 columns per row.
-        const int64_t row0 = (int64_t)tm * BM + wm + ty;
+        // Epilogue: rows wm+ty+8i (k-major A: wm+4ty+i, then wm+32+4ty+i-4),
+        // G runs of 4 columns per row; rows rise with i either way.
+        const int64_t row0 = (int64_t)tm * BM + wm + (Cfg::A_KMAJOR ? 4 * ty : ty);
         const int col0 = tn * BN + wn + tx * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int64_t row = row0 + 8 * i;
+            const int64_t row = row0 + (Cfg::A_KMAJOR ? (i < 4 ? i : 28 + i) : 8 * i);
             if (row >= M) break;
             float *crow = ep.C + (int64_t)bt * ep.stride_c + row * ep.ldc;
 #pragma unroll
@@ -369,6 +410,7 @@ using CfgFfma2_128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, 8, true, 1>;
 using CfgFfma2_128x128k16s8 = FfmaTmaCfg<128, 128, 16, 8, 8, true, 1>;
 using CfgFfma2_128x64k32s4 = FfmaTmaCfg<128, 64, 32, 4, 8, true, 2>;
 using CfgFfma2_128x256k32s4 = FfmaTmaCfg<128, 256, 32, 4, 16, true, 1>;
+using CfgFfma2_128x256k32s4ka = FfmaTmaCfg<128, 256, 32, 4, 16, true, 1, true>;
 
 std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
@@ -443,8 +485,12 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     // An operand with batch stride 0 is one matrix shared by every entry.
     const int a_bz = (g.batch > 1 && g.stride_a != 0) ? 1 : 0;
     const int b_bz = (g.batch > 1 && g.stride_b != 0) ? 1 : 0;
-    cudaError_t e = encode_3d(&mapA, g.A, g.M, g.K, g.lda, a_bz ? g.batch : 1, g.stride_a, Cfg::BM, Cfg::BK,
-                              Cfg::A_SWIZZLE);
+    // A is M x K, or K x M for a k-major configuration (boxes of BK rows of BM).
+    cudaError_t e = Cfg::A_KMAJOR
+                        ? encode_3d(&mapA, g.A, g.K, g.M, g.lda, a_bz ? g.batch : 1, g.stride_a, Cfg::BK, Cfg::BM,
+                                    Cfg::A_SWIZZLE)
+                        : encode_3d(&mapA, g.A, g.M, g.K, g.lda, a_bz ? g.batch : 1, g.stride_a, Cfg::BM, Cfg::BK,
+                                    Cfg::A_SWIZZLE);
     if (e != cudaSuccess) return e;
     e = encode_3d(&mapB, g.B, g.K, g.N, g.ldb, b_bz ? g.batch : 1, g.stride_b, Cfg::BK, Cfg::BN,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -483,6 +529,7 @@ cudaError_t prepare_ffma_tma()
     if ((e = set_smem_limit<CfgFfma2_128x128k32s4>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x128k16s8>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x64k32s4>()) != cudaSuccess) return e;
+    if ((e = set_smem_limit<CfgFfma2_128x256k32s4ka>()) != cudaSuccess) return e;
     return set_smem_limit<CfgFfma2_128x256k32s4>();
 }
 
@@ -494,19 +541,24 @@ size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
     case kKernFfma2_128x128k16s8: return workspace_bytes<CfgFfma2_128x128k16s8>(make_schedule<CfgFfma2_128x128k16s8>(g, true));
     case kKernFfma2_128x64k32s4: return workspace_bytes<CfgFfma2_128x64k32s4>(make_schedule<CfgFfma2_128x64k32s4>(g, true));
     case kKernFfma2_128x256k32s4: return workspace_bytes<CfgFfma2_128x256k32s4>(make_schedule<CfgFfma2_128x256k32s4>(g, true));
+    case kKernFfma2_128x256k32s4ka: return workspace_bytes<CfgFfma2_128x256k32s4ka>(make_schedule<CfgFfma2_128x256k32s4ka>(g, true));
     default: return 0;
     }
 }
 
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
 {
-    if (g.op_a != 0 || g.op_b != 0) return cudaErrorInvalidValue;   // transposed operands arrive packed
+    // B arrives K x N (transposed ones packed); A arrives M x K, except for
+    // the k-major configuration, which takes it K x M (op_a 1).
+    const int want_op_a = kernel == kKernFfma2_128x256k32s4ka ? 1 : 0;
+    if (g.op_a != want_op_a || g.op_b != 0) return cudaErrorInvalidValue;
     switch (kernel) {
     case kKernFfma128x128k32s4: return launch<CfgFfma128x128k32s4>(g, stream);
     case kKernFfma2_128x128k32s4: return launch<CfgFfma2_128x128k32s4>(g, stream);
     case kKernFfma2_128x128k16s8: return launch<CfgFfma2_128x128k16s8>(g, stream);
     case kKernFfma2_128x64k32s4: return launch<CfgFfma2_128x64k32s4>(g, stream);
     case kKernFfma2_128x256k32s4: return launch<CfgFfma2_128x256k32s4>(g, stream);
+    case kKernFfma2_128x256k32s4ka: return launch<CfgFfma2_128x256k32s4ka>(g, stream);
     default: return cudaErrorInvalidValue;
     }
 }

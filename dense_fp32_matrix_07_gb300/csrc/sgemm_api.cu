@@ -169,7 +169,8 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_
     const int cfg = select_config(p);
     const bool packs = kConfigTable[cfg].packs;
     if (out_config) *out_config = cfg;
-    if (out_pack_a) *out_pack_a = (packs && needs_pack(a_addr, lda)) ? 1 : 0;
+    // A k-major configuration always transposes the caller's M x K A.
+    if (out_pack_a) *out_pack_a = (packs && (kConfigTable[cfg].a_kmajor || needs_pack(a_addr, lda))) ? 1 : 0;
     if (out_pack_b) *out_pack_b = (packs && needs_pack(b_addr, ldb)) ? 1 : 0;
     return SGEMM_OK;
 }
@@ -256,6 +257,9 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     // The automatic choice for tiny products is a plain-form-only kernel of
     // the pages' ladder; the general form takes the smallest TMA tiles instead.
     if (c.config < 0 && !plain && !kConfigTable[cfg].uses_tma) cfg = kCfgFfma2_128x64;
+    // An A stored transposed (K x M) is what the k-major configuration reads
+    // in place, with no transposing pack: take it whenever 128 x 256 tiles are.
+    if (c.config < 0 && c.op_a == 1 && cfg == kCfgFfma2_128x256) cfg = kCfgFfma2_128x256_ka;
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
     // Kernels without TMA (the simple and ladder kernels) run the plain form only.
     if (!plain && !kConfigTable[cfg].uses_tma) return SGEMM_ERR_UNSUPPORTED;
@@ -277,17 +281,23 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     // rows and batch strides are 16-byte multiples on a 16-byte-aligned base;
     // anything else (a transposed operand included) is packed into scratch,
     // rows padded to 32 floats. A shared operand (batch stride 0) is packed once.
+    // A k-major configuration takes A stored K x M instead: in place when the
+    // caller stores it so (op_a 1) on those terms, else transposed (a plain
+    // A) or copied (a misaligned transposed one) into scratch.
     const bool packs = kConfigTable[cfg].packs;
+    const bool akm = kConfigTable[cfg].a_kmajor;
     auto stride_ok = [&](int64_t s, int64_t one) { return c.batch <= 1 || s == 0 || (s % 4 == 0 && s >= one); };
-    const bool pa = packs && (c.op_a == 1 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.M * c.lda));
+    const bool pa = packs && (akm ? (c.op_a == 0 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.K * c.lda))
+                                  : (c.op_a == 1 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.M * c.lda)));
     const bool pb = packs && (c.op_b == 1 || needs_pack(b, c.ldb) || !stride_ok(c.sb, c.K * c.ldb));
-    const int64_t lda_p = round_up(c.K, 32), ldb_p = round_up(c.N, 32);
+    const int64_t a_rows_p = akm ? c.K : c.M;                       // rows of the packed A
+    const int64_t lda_p = round_up(akm ? c.M : c.K, 32), ldb_p = round_up(c.N, 32);
     const int64_t a_entries = (c.batch > 1 && c.sa != 0) ? c.batch : 1;
     const int64_t b_entries = (c.batch > 1 && c.sb != 0) ? c.batch : 1;
-    const size_t a_bytes = pa ? (size_t)(a_entries * c.M * lda_p) * 4 : 0;
+    const size_t a_bytes = pa ? (size_t)(a_entries * a_rows_p * lda_p) * 4 : 0;
     const size_t b_bytes = pb ? (size_t)(b_entries * c.K * ldb_p) * 4 : 0;
     const size_t ws_off = (a_bytes + b_bytes + 255) / 256 * 256;
-    if (pa) g.op_a = 0;
+    if (pa) g.op_a = akm ? 1 : 0;
     if (pb) g.op_b = 0;
     const size_t ws_bytes = config_workspace_bytes(cfg, g);
     const size_t total = ws_off + ws_bytes;
@@ -300,13 +310,14 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
         cudaError_t e = cudaSuccess;
         if (pa) {
             float *dst = reinterpret_cast<float *>(scratch);
-            e = c.op_a == 1 ? launch_pack_transpose_batched(c.A, c.K, c.M, c.lda, c.sa, dst, lda_p, c.M * lda_p,
-                                                            a_entries, stream)
-                            : launch_pack_batched(c.A, c.M, c.K, c.lda, c.sa, dst, lda_p, c.M * lda_p, a_entries,
-                                                  stream);
+            const bool transpose = akm ? c.op_a == 0 : c.op_a == 1;
+            e = transpose ? launch_pack_transpose_batched(c.A, a_rows, a_cols, c.lda, c.sa, dst, lda_p,
+                                                          a_rows_p * lda_p, a_entries, stream)
+                          : launch_pack_batched(c.A, a_rows, a_cols, c.lda, c.sa, dst, lda_p, a_rows_p * lda_p,
+                                                a_entries, stream);
             g.A = dst;
             g.lda = lda_p;
-            g.stride_a = a_entries > 1 ? c.M * lda_p : 0;
+            g.stride_a = a_entries > 1 ? a_rows_p * lda_p : 0;
         }
         if (e == cudaSuccess && pb) {
             float *dst = reinterpret_cast<float *>(scratch + a_bytes);

@@ -168,6 +168,12 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     int cfg = -1, pack_a = 0, pack_b = 0;
     rc = sgemm_plan(M, N, K, lda, ldb, ldc, a, b, c, dev->num_sms, &cfg, &pack_a, &pack_b);
     if (rc != SGEMM_OK) return rc;
+    // A configuration that takes A k-major would need scratch for the whole
+    // transposed A; this entry point runs its twin that reads A as stored.
+    if (kConfigTable[cfg].a_kmajor) {
+        cfg = kCfgFfma2_128x256;
+        pack_a = ((a & 15u) != 0 || lda % 4 != 0) ? 1 : 0;
+    }
     const int64_t lda_p = round_up32(K), ldb_p = round_up32(N);
     const int64_t a_floats = pack_a ? M * lda_p : 0;
     const int64_t b_floats = pack_b ? K * ldb_p : 0;

@@ -40,6 +40,9 @@
 //      multiplicand with the one before)
 //  22  as 6, column serpentine over each half of the rows in turn
 //  23  as 6, column serpentine, b pairs in reverse order on odd k
+//  24  8 x 16 loop with the A slab k-major (one LDS.128 gives 4 rows at
+//      one k), column serpentine
+//  25  as 24, row-major order
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -365,12 +368,67 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
 template <int TN, int WM = 2>
 constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 
+// 24 / 25: the 8 x 16 loop with the A slab stored k-major, [32][128]
+// floats (M contiguous). Thread row ty owns rows 4ty..4ty+3 and
+// 32+4ty..32+4ty+3 of its warp's 64, so per k two conflict-free LDS.128
+// give its 8 A values in consecutive registers (with the row-major slab,
+// the 8 values of one k sit 4 registers apart). B as in 6.
+template <int ORDER>
+__global__ void __launch_bounds__(256, 1) inner_kmajor_kernel(float *out, int iters, unsigned long long *clk)
+{
+    constexpr int TN = 16, BM = 128, BN = 256, NT = 256;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float *sA = reinterpret_cast<float *>(smem);                 // [32][BM]
+    float *sB = reinterpret_cast<float *>(smem + 32 * BM * 4);   // [32][BN]
+    for (int e = threadIdx.x; e < BM * 32; e += NT) sA[e] = (e % 7) * 0.25f - 0.5f;
+    for (int e = threadIdx.x; e < BN * 32; e += NT) sB[e] = (e % 5) * 0.125f - 0.25f;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wm = (warp / 4) * 64, wn = (warp % 4) * 64;
+    const int ty = lane / 4, tx = lane % 4;
+    const char *As = reinterpret_cast<const char *>(sA) + (wm + 4 * ty) * 4;
+    const char *Bs = reinterpret_cast<const char *>(sB) + (wn + tx * 4) * 4;
+    float2 acc[8][TN / 2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+    const long long c0 = clock64();
+    const unsigned long long t0 = global_ns();
+    for (int it = 0; it < iters; ++it) {
+        unsigned z;
+        asm volatile("mov.u32 %0, 0;" : "=r"(z));
+        const char *Ai = As + z, *Bi = Bs + z;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float4 lo = *reinterpret_cast<const float4 *>(Ai + k * BM * 4);
+            const float4 hi = *reinterpret_cast<const float4 *>(Ai + k * BM * 4 + 128);
+            const float ak[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            float2 b2[TN / 2];
+#pragma unroll
+            for (int g = 0; g < TN / 4; ++g) {
+                const float4 v = *reinterpret_cast<const float4 *>(Bi + k * BN * 4 + g * 64);
+                b2[2 * g] = make_float2(v.x, v.y);
+                b2[2 * g + 1] = make_float2(v.z, v.w);
+            }
+            outer_step<ORDER>(acc, ak, b2, k);
+        }
+    }
+    record(clk, c0, t0);
+    float s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) s += acc[i][j].x + acc[i][j].y;
+    out[blockIdx.x * NT + threadIdx.x] = s;
+}
+
 }  // namespace
 
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 24; }
+int fma_probe_count(void) { return 26; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -383,7 +441,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 23 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 25 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -418,6 +476,8 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 21: inner_kernel<16, 2, false, 3><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 22: inner_kernel<16, 2, false, 4><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 23: inner_kernel<16, 2, false, 5><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 24: inner_kmajor_kernel<2><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 25: inner_kmajor_kernel<0><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
@@ -450,6 +510,12 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
                                  inner_smem<16>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kmajor_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kmajor_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);

@@ -73,9 +73,14 @@ def test_plan_validates_sizes(args, code):
 
 
 def test_plan_packs_only_misaligned_operands():
-    # Aligned operands with 16-byte rows: read in place.
+    # Aligned operands with 16-byte rows: read in place by the row-major
+    # 128x256 configuration (N below 2048)...
+    rc, cfg, pa, pb = sg.sgemm_plan(65536, 1024, 1024, 1024, 1024, 1024, 0, 0, 0, 148)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == "ffma2_128x256_k32_s4" and (pa, pb) == (0, 0)
+    # ...while the k-major configuration (N >= 2048) reads B in place and
+    # transposes A into scratch.
     rc, cfg, pa, pb = sg.sgemm_plan(4096, 4096, 4096, 4096, 4096, 4096, 0, 0, 0, 148)
-    assert rc == 0 and (pa, pb) == (0, 0)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == "ffma2_128x256_k32_s4_ka" and (pa, pb) == (1, 0)
     # Rows that are not a multiple of 16 bytes (the 4097x3001x2049 workload).
     rc, cfg, pa, pb = sg.sgemm_plan(4097, 3001, 2049, 2049, 3001, 3001, 0, 0, 0, 148)
     assert rc == 0 and (pa, pb) == (1, 1)
@@ -96,7 +101,7 @@ def test_plan_packs_only_misaligned_operands():
     (512, "ffma2_128x64_k32_s4"),       # 16 tiles of 128x128: the smallest TMA tiles
     (1024, "ffma2_128x128_k32_s4"),     # 64 tiles of 128x128 (>= a third of the SMs)
     (2048, "ffma2_128x128_k32_s4"),     # 128 tiles of 128x256 < 148 SMs
-    (4096, "ffma2_128x256_k32_s4"),     # 512 tiles of 128x256
+    (4096, "ffma2_128x256_k32_s4_ka"),  # 512 tiles of 128x256, N >= 2048: A k-major
 ])
 def test_plan_tile_size_follows_the_problem(n, name):
     rc, cfg, *_ = sg.sgemm_plan(n, n, n, n, n, n, 0, 0, 0, 148)

@@ -13,7 +13,8 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 IDS = sg.config_ids()
-CONFIGS = [-1, IDS["ffma2_128x128_k32_s4"], IDS["ffma2_128x256_k32_s4_sk"], IDS["ffma2_128x128_k32_s4_sk"],
+CONFIGS = [-1, IDS["ffma2_128x128_k32_s4"], IDS["ffma2_128x256_k32_s4_sk"], IDS["ffma2_128x256_k32_s4_ka"],
+           IDS["ffma2_128x128_k32_s4_sk"],
            IDS["ffma_128x128_k32_s4"], IDS["tf32x3_128x256_k16_s4"], IDS["tf32x3_128x256_k16_s4_sk"],
            IDS["tf32x3_pair_128x256_k16_s4"]]
 CFG_IDS = ["auto" if c < 0 else sg.sgemm_config_name(c) for c in CONFIGS]
@@ -94,8 +95,9 @@ def test_integer_exact_with_alpha_beta(cuda_device, oracle, config):
     _check(oracle, 1, 0, M, N, K, 2.0, -1.0, batch, A, B, Cin, out, lds, exact=True)
 
 
-@pytest.mark.parametrize("config", [-1, IDS["ffma2_128x256_k32_s4"], IDS["tf32x3_128x256_k16_s4"]],
-                         ids=["auto", "ffma2_128x256", "tf32x3"])
+@pytest.mark.parametrize("config", [-1, IDS["ffma2_128x256_k32_s4"], IDS["ffma2_128x256_k32_s4_ka"],
+                                    IDS["tf32x3_128x256_k16_s4"]],
+                         ids=["auto", "ffma2_128x256", "ffma2_128x256_ka", "tf32x3"])
 @pytest.mark.parametrize("shared", [(True, False), (False, True)], ids=["shared_A", "shared_B"])
 def test_shared_operand_across_the_batch(cuda_device, oracle, config, shared):
     M, N, K, batch = 300, 260, 130, 4

@@ -15,8 +15,8 @@ pytestmark = pytest.mark.gpu
 IDS = sg.config_ids()
 
 
-@pytest.mark.parametrize("config_name", [None, "ffma2_128x256_k32_s4_sk", "ffma2_128x128_k32_s4",
-                                         "tf32x3_pair_128x256_k16_s4"])
+@pytest.mark.parametrize("config_name", [None, "ffma2_128x256_k32_s4_sk", "ffma2_128x256_k32_s4_ka",
+                                         "ffma2_128x128_k32_s4", "tf32x3_pair_128x256_k16_s4"])
 def test_captured_products_replay_correctly(cuda_device, oracle, config_name):
     M, N, K = 700, 900, 515          # several tiles, ragged edges, stream-K tail on the auto path
     config = -1 if config_name is None else IDS[config_name]

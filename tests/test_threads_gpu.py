@@ -26,6 +26,7 @@ def test_concurrent_calls_on_separate_streams(cuda_device, oracle):
         (1024, 1024, 1024, 1024, IDS["ffma2_128x128_k32_s4_sk"]),
         (300, 257, 129, 129, -1),
         (700, 900, 515, 515, IDS["tf32x3_pair_128x256_k16_s4"]),
+        (640, 520, 300, 301, IDS["ffma2_128x256_k32_s4_ka"]),
     ]
     inputs, refs = [], []
     for n, (M, N, K, lda, _) in enumerate(jobs):
