@@ -564,6 +564,10 @@ def main():
         dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
         rc, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(),
                                         dB.data_ptr(), dC.data_ptr(), num_sms)
+        if args.noalloc and sg.sgemm_config_name(cfg).endswith("_ka"):
+            # sgemm_noalloc runs the twin that reads A as stored (no scratch for A).
+            cfg = sg.config_ids()["ffma2_128x256_k32_s4"]
+            pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
         launches_per_step = 1 + pa + pb
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
         flops = product_flops(w.M, w.N, w.K)
@@ -589,12 +593,17 @@ def main():
         dB = gB.reshape(1, -1).to(dev).repeat(args.batch, 1)
         dC = torch.ones((args.batch, w.M, w.N), dtype=torch.float32, device=dev)
         cfg = args.config
+        ids = sg.config_ids()
         if cfg < 0:
+            # The general form's automatic choice, as the library makes it.
             rc, cfg, _, _ = sg.sgemm_plan(w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, num_sms)
             if not sg.sgemm_config_name(cfg).startswith(("ffma", "tf32")):
-                cfg = sg.config_ids()["ffma2_128x64_k32_s4"]     # the general form's choice for tiny products
+                cfg = ids["ffma2_128x64_k32_s4"]     # tiny products take the smallest TMA tiles
+            if args.op_a == 1 and cfg == ids["ffma2_128x256_k32_s4"]:
+                cfg = ids["ffma2_128x256_k32_s4_ka"]  # reads a transposed A in place
         packs = sg.sgemm_config_name(cfg).startswith("ffma")
-        pa = int(packs and (args.op_a == 1 or lda_g % 4 != 0))
+        a_kmajor = sg.sgemm_config_name(cfg).endswith("_ka")
+        pa = int(packs and (((args.op_a == 0) if a_kmajor else (args.op_a == 1)) or lda_g % 4 != 0))
         pb = int(packs and (args.op_b == 1 or ldb_g % 4 != 0))
         launches_per_step = (1 + pa + pb) if packs else 3 * args.batch
         total_bytes = 4 * args.batch * (sa + sb + sc)
