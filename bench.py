@@ -567,7 +567,7 @@ def main():
                                         dB.data_ptr(), dC.data_ptr(), num_sms)
         if args.noalloc and sg.sgemm_config_name(cfg).endswith("_ka"):
             # sgemm_noalloc runs the twin that reads A as stored (no scratch for A).
-            cfg = sg.config_ids()["ffma2_128x256_k32_s4"]
+            cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
             pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
         launches_per_step = 1 + pa + pb
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
@@ -600,8 +600,8 @@ def main():
             rc, cfg, _, _ = sg.sgemm_plan(w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, num_sms)
             if not sg.sgemm_config_name(cfg).startswith(("ffma", "tf32")):
                 cfg = ids["ffma2_128x64_k32_s4"]     # tiny products take the smallest TMA tiles
-            if args.op_a == 1 and cfg == ids["ffma2_128x256_k32_s4"]:
-                cfg = ids["ffma2_128x256_k32_s4_ka"]  # reads a transposed A in place
+            if args.op_a == 1 and sg.sgemm_config_name(cfg) in ("ffma2_128x256_k32_s4", "ffma2_128x128_k32_s4"):
+                cfg = ids[sg.sgemm_config_name(cfg) + "_ka"]  # reads a transposed A in place
         packs = sg.sgemm_config_name(cfg).startswith("ffma")
         a_kmajor = sg.sgemm_config_name(cfg).endswith("_ka")
         pa = int(packs and (((args.op_a == 0) if a_kmajor else (args.op_a == 1)) or lda_g % 4 != 0))

@@ -25,6 +25,7 @@ enum KernelId : int {
     kKernFfma2_128x64k32s4,     // 128x64 block (4 consumer warps), 2 CTAs per SM
     kKernFfma2_128x256k32s4,    // 128x256 block, 8x16 thread tiles, FFMA2
     kKernFfma2_128x256k32s4ka,  // the same with A stored K x M (k-major slabs)
+    kKernFfma2_128x128k32s4ka,  // the 128x128 FFMA2 block with A stored K x M
     // The pages' kernel ladder (kernels_ladder.cu), for measurement.
     kKernLadderNaive,           // one thread per output, threadIdx.x -> row
     kKernLadderCoalesced,       // one thread per output, threadIdx.x -> column
@@ -60,6 +61,7 @@ enum ConfigId : int {
     kCfgTf32x3_pair,
     kCfgTf32x3_pair_dp,
     kCfgFfma2_128x256_ka,
+    kCfgFfma2_128x128_ka,
     kNumConfigs
 };
 

@@ -407,6 +407,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
 // Configurations: <BM, BN, BK, STAGES, TN, PAIRED, MIN_BLOCKS>.
 using CfgFfma128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, 8, false, 1>;
 using CfgFfma2_128x128k32s4 = FfmaTmaCfg<128, 128, 32, 4, 8, true, 1>;
+using CfgFfma2_128x128k32s4ka = FfmaTmaCfg<128, 128, 32, 4, 8, true, 1, true>;
 using CfgFfma2_128x128k16s8 = FfmaTmaCfg<128, 128, 16, 8, 8, true, 1>;
 using CfgFfma2_128x64k32s4 = FfmaTmaCfg<128, 64, 32, 4, 8, true, 2>;
 using CfgFfma2_128x256k32s4 = FfmaTmaCfg<128, 256, 32, 4, 16, true, 1>;
@@ -530,6 +531,7 @@ cudaError_t prepare_ffma_tma()
     if ((e = set_smem_limit<CfgFfma2_128x128k16s8>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x64k32s4>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x256k32s4ka>()) != cudaSuccess) return e;
+    if ((e = set_smem_limit<CfgFfma2_128x128k32s4ka>()) != cudaSuccess) return e;
     return set_smem_limit<CfgFfma2_128x256k32s4>();
 }
 
@@ -542,6 +544,7 @@ size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
     case kKernFfma2_128x64k32s4: return workspace_bytes<CfgFfma2_128x64k32s4>(make_schedule<CfgFfma2_128x64k32s4>(g, true));
     case kKernFfma2_128x256k32s4: return workspace_bytes<CfgFfma2_128x256k32s4>(make_schedule<CfgFfma2_128x256k32s4>(g, true));
     case kKernFfma2_128x256k32s4ka: return workspace_bytes<CfgFfma2_128x256k32s4ka>(make_schedule<CfgFfma2_128x256k32s4ka>(g, true));
+    case kKernFfma2_128x128k32s4ka: return workspace_bytes<CfgFfma2_128x128k32s4ka>(make_schedule<CfgFfma2_128x128k32s4ka>(g, true));
     default: return 0;
     }
 }
@@ -549,8 +552,8 @@ size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
 {
     // B arrives K x N (transposed ones packed); A arrives M x K, except for
-    // the k-major configuration, which takes it K x M (op_a 1).
-    const int want_op_a = kernel == kKernFfma2_128x256k32s4ka ? 1 : 0;
+    // the k-major configurations, which take it K x M (op_a 1).
+    const int want_op_a = (kernel == kKernFfma2_128x256k32s4ka || kernel == kKernFfma2_128x128k32s4ka) ? 1 : 0;
     if (g.op_a != want_op_a || g.op_b != 0) return cudaErrorInvalidValue;
     switch (kernel) {
     case kKernFfma128x128k32s4: return launch<CfgFfma128x128k32s4>(g, stream);
@@ -559,6 +562,7 @@ cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
     case kKernFfma2_128x64k32s4: return launch<CfgFfma2_128x64k32s4>(g, stream);
     case kKernFfma2_128x256k32s4: return launch<CfgFfma2_128x256k32s4>(g, stream);
     case kKernFfma2_128x256k32s4ka: return launch<CfgFfma2_128x256k32s4ka>(g, stream);
+    case kKernFfma2_128x128k32s4ka: return launch<CfgFfma2_128x128k32s4ka>(g, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -257,9 +257,11 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     // The automatic choice for tiny products is a plain-form-only kernel of
     // the pages' ladder; the general form takes the smallest TMA tiles instead.
     if (c.config < 0 && !plain && !kConfigTable[cfg].uses_tma) cfg = kCfgFfma2_128x64;
-    // An A stored transposed (K x M) is what the k-major configuration reads
-    // in place, with no transposing pack: take it whenever 128 x 256 tiles are.
+    // An A stored transposed (K x M) is what the k-major configurations read
+    // in place, with no transposing pack: take them whenever their row-major
+    // twins would run.
     if (c.config < 0 && c.op_a == 1 && cfg == kCfgFfma2_128x256) cfg = kCfgFfma2_128x256_ka;
+    if (c.config < 0 && c.op_a == 1 && cfg == kCfgFfma2_128x128) cfg = kCfgFfma2_128x128_ka;
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
     // Kernels without TMA (the simple and ladder kernels) run the plain form only.
     if (!plain && !kConfigTable[cfg].uses_tma) return SGEMM_ERR_UNSUPPORTED;

@@ -171,7 +171,7 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     // A configuration that takes A k-major would need scratch for the whole
     // transposed A; this entry point runs its twin that reads A as stored.
     if (kConfigTable[cfg].a_kmajor) {
-        cfg = kCfgFfma2_128x256;
+        cfg = cfg == kCfgFfma2_128x128_ka ? kCfgFfma2_128x128 : kCfgFfma2_128x256;
         pack_a = ((a & 15u) != 0 || lda % 4 != 0) ? 1 : 0;
     }
     const int64_t lda_p = round_up32(K), ldb_p = round_up32(N);

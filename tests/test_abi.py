@@ -100,7 +100,7 @@ def test_plan_packs_only_misaligned_operands():
     (384, "ladder_register_tiled_2x2"),
     (512, "ffma2_128x64_k32_s4"),       # 16 tiles of 128x128: the smallest TMA tiles
     (1024, "ffma2_128x128_k32_s4"),     # 64 tiles of 128x128 (>= a third of the SMs)
-    (2048, "ffma2_128x128_k32_s4"),     # 128 tiles of 128x256 < 148 SMs
+    (2048, "ffma2_128x128_k32_s4_ka"),  # 128 tiles of 128x256 < 148 SMs; N >= 2048: A k-major
     (4096, "ffma2_128x256_k32_s4_ka"),  # 512 tiles of 128x256, N >= 2048: A k-major
 ])
 def test_plan_tile_size_follows_the_problem(n, name):
