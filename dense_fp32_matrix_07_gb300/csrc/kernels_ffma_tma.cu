@@ -19,8 +19,12 @@
 // every consumer warp has finished with it), which replace the pages' two
 // __syncthreads() per phase. The A slab uses the TMA 128-byte (BK 32) or
 // 64-byte (BK 16) swizzle instead of the pages' +1 padding column, which
-// TMA cannot produce. Zero fill of out-of-range boxes by TMA handles the M, N
-// and K tails; the epilogue predicates its stores.
+// TMA cannot produce. The k-major configurations read A stored K x M
+// instead (a transposed copy, or the caller's transposed A): their slab is
+// [BK][BM], M contiguous, unswizzled, and one LDS.128 gives a thread 4 of
+// its rows at one k, in consecutive registers, which the FFMA2 loop issues
+// faster than values 4 registers apart. Zero fill of out-of-range boxes by
+// TMA handles the M, N and K tails; the epilogue predicates its stores.
 //
 // Work schedule (persistent grid, at most one CTA per SM and resident slot):
 // output tiles are numbered in groups of 8 block rows (so CTAs running at the

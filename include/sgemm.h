@@ -28,6 +28,7 @@
  * Ownership: every pointer is caller-owned device memory; the library never
  * frees, retains or reads host memory through it. Scratch space the library
  * needs (a packed copy of an operand whose rows are not 16-byte aligned, the
+ * transposed K x M copy of A that the k-major configurations read, the
  * partial sums and flags of a stream-K tail, the hi/lo operand planes of the
  * 3xTF32 configurations) is taken from a library-owned, stream-ordered
  * memory pool on `stream` and returned on `stream`; it is never exposed.
@@ -96,9 +97,13 @@ enum {
  * Any alignment of A, B, C and any leading dimension is accepted. Operands
  * whose base address is 16-byte aligned and whose leading dimension is a
  * multiple of 4 floats are read in place by the tensor-memory-accelerator
- * (TMA) path; others are first packed into aligned scratch. C is written with
- * 16-byte vector stores when it is aligned the same way, else with scalar
- * stores.
+ * (TMA) path; others are first packed into aligned scratch. For products of
+ * 128x256 or 128x128 tiles with N >= 2048 the automatic choice is a k-major
+ * configuration ("ffma2_128x256_k32_s4_ka", "ffma2_128x128_k32_s4_ka"),
+ * whose kernel reads A as a K x M matrix: A is first transposed into
+ * scratch (K * round_up(M, 32) floats, about 8*M*K bytes of traffic), which
+ * its faster inner loop repays. C is written with 16-byte vector stores when
+ * it is aligned the same way, else with scalar stores.
  *
  * Returns SGEMM_OK or one of the codes above. A device-side timeout cannot
  * be known when the call returns; see sgemm_check_status().
@@ -149,8 +154,12 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K,
  *
  * Pointers are device pointers; C must not overlap A or B (over the whole
  * batch). Transposed operands and rows or batch strides that are not 16-byte
- * multiples are packed into pool scratch first; alpha and beta are applied in
- * the kernels' epilogues; on the FFMA configurations batch entries share one
+ * multiples are packed into pool scratch first, except that the k-major
+ * configurations read a transposed A (stored K x M, aligned) in place and
+ * transpose a plain one; the automatic choice takes a k-major configuration
+ * for a transposed A wherever it would take its row-major twin. Alpha and
+ * beta are applied in the kernels' epilogues; on the FFMA configurations
+ * batch entries share one
  * persistent launch (their tiles are one schedule), on the 3xTF32 ones each
  * entry is split and multiplied in turn. Status codes as sgemm();
  * SGEMM_ERR_UNSUPPORTED if
@@ -198,7 +207,9 @@ const char *sgemm_config_name(int config);
  *   num_sms                  streaming multiprocessors of the target device.
  *   out_config               (nullable) receives the chosen configuration.
  *   out_pack_a, out_pack_b   (nullable) receive 1 if that operand would be
- *                            packed into scratch first, else 0.
+ *                            packed into scratch first (for A under a
+ *                            k-major configuration: always, transposed),
+ *                            else 0.
  *
  * Returns SGEMM_OK, or the code sgemm() would return for invalid sizes.
  */
@@ -285,7 +296,9 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
  * such operands into a fixed scratch array compiled into the library instead,
  * keeps the stream-K partial sums and flags in a second fixed array (24 MiB;
  * a schedule needing more, on GPUs of over 190 SMs, runs whole tiles), and
- * allocates nothing.
+ * allocates nothing. Where sgemm() would take a k-major configuration, which
+ * needs scratch for the whole transposed A, this entry point runs that
+ * configuration's twin that reads A as stored.
  *
  * Arguments, semantics, ownership and status codes: as sgemm().
  *
