@@ -17,13 +17,17 @@
 // the product's schedule (at most one 128 x 256 tile per SM: about 19 MiB on
 // 152 SMs); a schedule that would need more runs whole tiles instead.
 //
+// Where sgemm() would take a k-major configuration (one that reads A as a
+// transposed copy, which needs scratch for the whole of A), this entry point
+// runs that configuration's twin, which reads A as stored.
+//
 // Sharing: every call on a device uses the same arrays, which keep whatever
 // the last call left in them. Nothing in it has to start at zero (each call
 // rewrites every packed entry the product reads, the padding at the end of
 // packed rows is never read, and the stream-K flags are zeroed by a memset on
-// the call's stream before its product). Calls whose work overlaps on the GPU (different
-// streams, or different host threads) race on the array and must be ordered
-// by the caller.
+// the call's stream before its product). Calls whose work overlaps on the
+// GPU (different streams, or different host threads) race on the array and
+// must be ordered by the caller.
 #include "../../include/sgemm.h"
 #include "common.cuh"
 #include "configs.cuh"
