@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 
 IDS = sg.config_ids()
 FAMILIES = [-1, IDS["ffma2_128x64_k32_s4"], IDS["ffma2_128x128_k32_s4_sk"], IDS["ffma2_128x256_k32_s4"],
-            IDS["ffma2_128x256_k32_s4_ka"], IDS["ffma2_128x128_k32_s4_ka"], IDS["ffma_128x128_k32_s4"], IDS["tf32x3_128x256_k16_s4"], IDS["tf32x3_pair_128x256_k16_s4"]]
+            IDS["ffma2_128x256_k32_s4_ka"], IDS["ffma2_128x128_k32_s4_ka"], IDS["ffma_128x128_k32_s4"],
+            IDS["tf32x3_128x256_k16_s4"], IDS["tf32x3_pair_128x256_k16_s4"]]
 CASES_PER_FAMILY = 10
 
 
