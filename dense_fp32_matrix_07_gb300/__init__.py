@@ -32,7 +32,7 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
             "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_test_schedule",
-            "sgemm_general", "sgemm_general_ex")
+            "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,8 @@ def load(rebuild: bool = False):
             lib.sgemm_test_schedule.restype = ctypes.c_int
             lib.sgemm_test_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64,
                                                 ctypes.c_int, _i64, _vp, _i64, _vp, _vp]
+            lib.sgemm_test_fail_next_allocs.restype = ctypes.c_int
+            lib.sgemm_test_fail_next_allocs.argtypes = [ctypes.c_int]
             lib.sgemm_test_launch_without_cluster.restype = ctypes.c_int
             lib.sgemm_test_launch_without_cluster.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                                               _vp, _i64, _vp]
@@ -116,6 +118,11 @@ def sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     stream-K partial sums go in a fixed 24 MiB array. All calls on a device
     share those arrays, so calls that overlap on the GPU race on them."""
     return load().sgemm_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def sgemm_test_fail_next_allocs(n) -> int:
+    """Test hook: the next `n` scratch allocations are treated as failed (host only)."""
+    return load().sgemm_test_fail_next_allocs(n)
 
 
 def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) -> int:

@@ -6,6 +6,7 @@
 #include "configs.cuh"
 #include "schedule.cuh"
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -115,6 +116,18 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Test hook (sgemm_test_fail_next_allocs): scratch allocations still to fail.
+std::atomic<int> g_fail_allocs{0};
+
+// One pending test failure, if any is left to take.
+bool take_test_alloc_failure()
+{
+    int n = g_fail_allocs.load();
+    while (n > 0)
+        if (g_fail_allocs.compare_exchange_weak(n, n - 1)) return true;
+    return false;
+}
 
 }  // namespace
 
@@ -305,8 +318,17 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     const size_t total = ws_off + ws_bytes;
     uint8_t *scratch = nullptr;
     if (total > 0) {
-        if (cudaMallocFromPoolAsync((void **)&scratch, total, dev->pool, stream) != cudaSuccess) {
+        if (take_test_alloc_failure() ||
+            cudaMallocFromPoolAsync((void **)&scratch, total, dev->pool, stream) != cudaSuccess) {
             cudaGetLastError();
+            // An automatic k-major choice needs scratch for the whole
+            // transposed A; when that cannot be had, the row-major twin
+            // (which reads an aligned A as stored) runs the product instead.
+            if (c.config < 0 && akm && c.op_a == 0) {
+                Call twin = c;
+                twin.config = cfg == kCfgFfma2_128x128_ka ? kCfgFfma2_128x128 : kCfgFfma2_128x256;
+                return sgemm_call(twin, stream);
+            }
             return SGEMM_ERR_ALLOC;
         }
         cudaError_t e = cudaSuccess;
@@ -384,6 +406,13 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K, const float *A, in
     // waits between CTAs, only the withheld copy.
     return sgemm_impl(M, N, K, A, lda, B, ldb, C, ldc, kCfgFfma2_128x256, kSchedDataParallel,
                       slab < 0 ? -1 : slab, stream);
+}
+
+int sgemm_test_fail_next_allocs(int n)
+{
+    if (n < 0) return SGEMM_ERR_INVALID_VALUE;
+    g_fail_allocs.store(n);
+    return SGEMM_OK;
 }
 
 int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,

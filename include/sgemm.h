@@ -261,6 +261,20 @@ int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
                                       float *C, int64_t ldc, cudaStream_t stream);
 
 /*
+ * sgemm_test_fail_next_allocs — test hook for the allocation-failure paths
+ * (the pages have no counterpart).
+ *
+ * The next n scratch allocations of sgemm(), sgemm_ex(), sgemm_general()
+ * and sgemm_general_ex() (in any thread) are treated as failed without
+ * asking the pool. An automatic k-major choice then falls back to its
+ * row-major twin, which reads an aligned A as stored; any other call whose
+ * allocation fails returns SGEMM_ERR_ALLOC with nothing enqueued. n = 0
+ * clears a pending count. Returns SGEMM_OK, or SGEMM_ERR_INVALID_VALUE for
+ * n < 0. Host only; needs no GPU.
+ */
+int sgemm_test_fail_next_allocs(int n);
+
+/*
  * sgemm_test_schedule — test hook (host only, no GPU): the work schedule the
  * persistent kernels follow, enumerated.
  *

@@ -129,3 +129,9 @@ def test_fma_probe_library_exports_its_entry_points():
     lib.fma_probe_count.restype = ctypes.c_int
     import bench
     assert lib.fma_probe_count() == len(bench.FMA_PROBES)
+
+
+def test_fail_next_allocs_hook_validates_its_count():
+    assert sg.sgemm_test_fail_next_allocs(-1) == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_test_fail_next_allocs(2) == sg.SGEMM_OK
+    assert sg.sgemm_test_fail_next_allocs(0) == sg.SGEMM_OK

@@ -2,7 +2,9 @@
 makes the kernel's bounded waits expire; the kernel reports a timeout through
 the device error word and exits, and the context stays usable. A cluster
 kernel launched without its cluster notices before it touches anything and
-reports a launch error."""
+reports a launch error. A scratch allocation that fails (made to, by a
+host-side test hook) sends an automatic k-major choice to its row-major
+twin."""
 
 import time
 
@@ -69,3 +71,37 @@ def test_cluster_kernel_refuses_a_launch_without_its_cluster(cuda_device, oracle
     assert sg.sgemm_check_status(s) == sg.SGEMM_OK
     Cref, S = oracle.sgemm(n, n, n, A.numpy(), n, B.numpy(), n)
     assert_parity(dC.matrix(), Cref, S, True, "pair kernel after the refused launch")
+
+
+def test_kmajor_choice_falls_back_when_its_scratch_cannot_be_had(cuda_device, oracle):
+    # N >= 2048 and enough 128x128 tiles: the automatic choice is a k-major
+    # configuration, which needs scratch for the transposed A. With that
+    # allocation failing, the row-major twin runs the product instead.
+    M, N, K = 512, 2048, 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rc, cfg, pa, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, sms)
+    assert rc == 0 and sg.sgemm_config_name(cfg).endswith("_ka") and pa == 1
+    A, B = workloads.make_operands(M, N, K, "int", 11)
+    dA, dB = DeviceMatrix(A, M, K, K), DeviceMatrix(B, K, N, N)
+    dC = DeviceMatrix(None, M, N, N)
+    s = torch.cuda.current_stream().cuda_stream
+    Cref, S = oracle.sgemm(M, N, K, A.numpy(), K, B.numpy(), N)
+    try:
+        assert sg.sgemm_test_fail_next_allocs(1) == sg.SGEMM_OK
+        assert sg.sgemm(M, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N, s) == sg.SGEMM_OK
+        assert sg.sgemm_check_status(s) == sg.SGEMM_OK
+        assert_parity(dC.matrix(), Cref, S, True, "row-major twin after the failed allocation")
+        # Forced, the k-major configuration has nowhere to go: it reports the
+        # failure and enqueues nothing (C keeps its sentinel).
+        dC2 = DeviceMatrix(None, M, N, N)
+        before = dC2.matrix().clone()
+        assert sg.sgemm_test_fail_next_allocs(1) == sg.SGEMM_OK
+        assert sg.sgemm_ex(M, N, K, dA.ptr, K, dB.ptr, N, dC2.ptr, N, cfg, s) == sg.SGEMM_ERR_ALLOC
+        torch.cuda.synchronize()
+        assert torch.equal(dC2.matrix().view(torch.int32), before.view(torch.int32))
+    finally:
+        sg.sgemm_test_fail_next_allocs(0)
+    # With no failure pending, the k-major configuration itself runs.
+    assert sg.sgemm_ex(M, N, K, dA.ptr, K, dB.ptr, N, dC.ptr, N, cfg, s) == sg.SGEMM_OK
+    assert sg.sgemm_check_status(s) == sg.SGEMM_OK
+    assert_parity(dC.matrix(), Cref, S, True, "k-major")
