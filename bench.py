@@ -862,7 +862,11 @@ def main():
                      "frac": round(achieved_tflops / peak_tflops, 4),
                      "traffic": traffic,
                      "peak_basis": f"{num_sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
-                                   f"{sm_max:.0f} MHz (max SM clock)"},
+                                   f"{sm_max:.0f} MHz (max SM clock)",
+                     "achieved_basis": ("2MNK / mean CUDA-event time of one call: the product kernel"
+                                        + (f" and its {launches_per_step - 1} operand pack(s)"
+                                           if launches_per_step > 1 else "")
+                                        + ", on the launching stream")},
         "clocks": clocks,
         "host_elapsed_s": round(elapsed_host, 3),
         "tensor_core_3xtf32": tc,

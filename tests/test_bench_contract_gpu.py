@@ -44,6 +44,8 @@ def test_bench_line_has_every_contract_field(cuda_device):
     assert roof["bound"] == "alu" and roof["unit"] == "TFLOP/s"
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
     assert 0 < roof["frac"] < 1.2
+    assert roof["achieved_basis"].startswith("2MNK / mean CUDA-event time of one call")
+    assert d["gpu_launches"] % d["steps"] == 0   # every step launches the same kernels
 
     cpu = d["cpu_baseline"]
     for key in ("value", "unit", "cores", "kind", "sample"):
