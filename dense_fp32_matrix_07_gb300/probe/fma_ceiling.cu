@@ -45,6 +45,8 @@
 //  25  as 24, row-major order
 //  26  the 8 x 8 loop (128 x 128 block) with the A slab k-major, column
 //      serpentine
+//  27  as 24 in the main kernel's launch shape: 384 threads, the third
+//      warpgroup leaving after setmaxnreg hands 232 registers to the others
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -375,16 +377,29 @@ constexpr int inner_smem() { return WM * 64 * 128 + 4 * 4 * TN * 128; }
 // 32+4ty..32+4ty+3 of its warp's 64, so per k two conflict-free LDS.128
 // give its 8 A values in consecutive registers (with the row-major slab,
 // the 8 values of one k sit 4 registers apart). B as in 6.
-template <int ORDER, int TN = 16>
-__global__ void __launch_bounds__(256, 1) inner_kmajor_kernel(float *out, int iters, unsigned long long *clk)
+template <int ORDER, int TN = 16, bool SPLIT = false>
+__global__ void __launch_bounds__(SPLIT ? 384 : 256, 1) inner_kmajor_kernel(float *out, int iters,
+                                                                            unsigned long long *clk)
 {
     constexpr int BM = 128, BN = 16 * TN, NT = 256;
     extern __shared__ __align__(1024) unsigned char smem[];
     float *sA = reinterpret_cast<float *>(smem);                 // [32][BM]
     float *sB = reinterpret_cast<float *>(smem + 32 * BM * 4);   // [32][BN]
-    for (int e = threadIdx.x; e < BM * 32; e += NT) sA[e] = (e % 7) * 0.25f - 0.5f;
-    for (int e = threadIdx.x; e < BN * 32; e += NT) sB[e] = (e % 5) * 0.125f - 0.25f;
+    if (threadIdx.x < NT) {
+        for (int e = threadIdx.x; e < BM * 32; e += NT) sA[e] = (e % 7) * 0.25f - 0.5f;
+        for (int e = threadIdx.x; e < BN * 32; e += NT) sB[e] = (e % 5) * 0.125f - 0.25f;
+    }
     __syncthreads();
+    if constexpr (SPLIT) {
+        // The main kernel's launch shape: a third warpgroup hands its
+        // registers to the two computing ones (40 / 232 of the 168 each
+        // thread was launched with) and leaves.
+        if (threadIdx.x >= NT) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+            return;
+        }
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wm = (warp / 4) * 64, wn = (warp % 4) * 4 * TN;
     const int ty = lane / 4, tx = lane % 4;
@@ -430,7 +445,7 @@ __global__ void __launch_bounds__(256, 1) inner_kmajor_kernel(float *out, int it
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 27; }
+int fma_probe_count(void) { return 28; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -443,7 +458,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 26 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 27 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -481,6 +496,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 24: inner_kmajor_kernel<2><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 25: inner_kmajor_kernel<0><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 26: inner_kmajor_kernel<2, 8><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
+        case 27: inner_kmajor_kernel<2, 16, true><<<sms, 384, inner_smem<16>()>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
@@ -488,7 +504,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     else if (kind <= 4 || kind == 8 || (kind >= 10 && kind <= 13)) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind >= 14 && kind <= 16) f = 2.0 * 128 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind == 5 || kind == 19 || kind == 20 || kind == 26) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else if (kind == 6 || kind == 9 || (kind >= 17 && kind <= 25)) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind == 6 || kind == 9 || (kind >= 17 && kind <= 25) || kind == 27) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
@@ -519,6 +535,9 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
                                  inner_smem<16>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kmajor_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kmajor_kernel<2, 16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
