@@ -147,3 +147,16 @@ def test_rejected_general_arguments(cuda_device):
     assert sg.sgemm_general(0, 0, 8, 8, 8, 1.0, p, 8, 0, p, 8, 0, 0.0, c, 8, 64, 0, s) == sg.SGEMM_OK  # empty batch
     torch.cuda.synchronize()
     assert bool((dC == 0).all())
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 64), (2048, 2560, 64)], ids=["128x128_tiles", "128x256_tiles"])
+def test_transposed_a_read_in_place_by_the_kmajor_configurations(cuda_device, oracle, M, N, K):
+    # Large enough for the automatic choice to take 128x128 or 128x256 tiles;
+    # for an A stored transposed on aligned rows (lda = M, a multiple of 4,
+    # tight batch stride) that means a k-major configuration reading it in
+    # place, with no pack. Integer inputs, so the result is exact.
+    batch = 2
+    rc, A, B, Cin, out, lds = _run(1, 0, M, N, K, 1.0, 0.0, batch, -1, dist="int", seed=9, pad=(0, 0, 0),
+                                   extra_stride=(0, 0, 0))
+    assert rc == 0
+    _check(oracle, 1, 0, M, N, K, 1.0, 0.0, batch, A, B, Cin, out, lds, exact=True)
