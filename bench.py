@@ -602,19 +602,13 @@ def main():
         dA = gA.reshape(1, -1).to(dev).repeat(args.batch, 1)
         dB = gB.reshape(1, -1).to(dev).repeat(args.batch, 1)
         dC = torch.ones((args.batch, w.M, w.N), dtype=torch.float32, device=dev)
-        cfg = args.config
-        ids = sg.config_ids()
-        if cfg < 0:
-            # The general form's automatic choice, as the library makes it.
-            rc, cfg, _, _ = sg.sgemm_plan(w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, num_sms)
-            if not sg.sgemm_config_name(cfg).startswith(("ffma", "tf32")):
-                cfg = ids["ffma2_128x64_k32_s4"]     # tiny products take the smallest TMA tiles
-            if args.op_a == 1 and sg.sgemm_config_name(cfg) in ("ffma2_128x256_k32_s4", "ffma2_128x128_k32_s4"):
-                cfg = ids[sg.sgemm_config_name(cfg) + "_ka"]  # reads a transposed A in place
+        # The configuration and operand packs of the step, as the library chooses them.
+        rc, cfg, pa, pb = sg.sgemm_general_plan(args.op_a, args.op_b, w.M, w.N, w.K, args.alpha, lda_g, sa, ldb_g,
+                                                sb, args.beta, ldc_g, sc, args.batch, dA.data_ptr(),
+                                                dB.data_ptr(), dC.data_ptr(), num_sms, args.config)
+        if rc != 0:
+            raise SystemExit(f"general form: {sg.sgemm_error_string(rc)}")
         packs = sg.sgemm_config_name(cfg).startswith("ffma")
-        a_kmajor = sg.sgemm_config_name(cfg).endswith("_ka")
-        pa = int(packs and (((args.op_a == 0) if a_kmajor else (args.op_a == 1)) or lda_g % 4 != 0))
-        pb = int(packs and (args.op_b == 1 or ldb_g % 4 != 0))
         launches_per_step = (1 + pa + pb) if packs else 3 * args.batch
         total_bytes = 4 * args.batch * (sa + sb + sc)
         flops = args.batch * product_flops(w.M, w.N, w.K)

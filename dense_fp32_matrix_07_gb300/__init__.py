@@ -32,7 +32,7 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
             "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_test_schedule",
-            "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex")
+            "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex", "sgemm_general_plan")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,12 @@ def load(rebuild: bool = False):
             lib.sgemm_general.argtypes = gen + [_vp]
             lib.sgemm_general_ex.restype = ctypes.c_int
             lib.sgemm_general_ex.argtypes = gen + [ctypes.c_int, _vp]
+            _pi = ctypes.POINTER(ctypes.c_int)
+            lib.sgemm_general_plan.restype = ctypes.c_int
+            lib.sgemm_general_plan.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_float,
+                                               _i64, _i64, _i64, _i64, ctypes.c_float, _i64, _i64, _i64,
+                                               ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
+                                               ctypes.c_int, _pi, _pi, _pi]
             lib.sgemm_check_status.restype = ctypes.c_int
             lib.sgemm_check_status.argtypes = [_vp]
             lib.sgemm_error_string.restype = ctypes.c_char_p
@@ -197,6 +203,17 @@ def sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms):
     cfg, pa, pb = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
     rc = load().sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms,
                            ctypes.byref(cfg), ctypes.byref(pa), ctypes.byref(pb))
+    return rc, cfg.value, pa.value, pb.value
+
+
+def sgemm_general_plan(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b, beta, ldc, stride_c,
+                       batch, a_addr, b_addr, c_addr, num_sms, config=-1):
+    """Host-only: (status, config, pack_a, pack_b) that sgemm_general_ex() would use
+    (config -1 when the call runs no product)."""
+    cfg, pa, pb = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    rc = load().sgemm_general_plan(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b, beta, ldc,
+                                   stride_c, batch, a_addr, b_addr, c_addr, num_sms, config,
+                                   ctypes.byref(cfg), ctypes.byref(pa), ctypes.byref(pb))
     return rc, cfg.value, pa.value, pb.value
 
 

@@ -220,13 +220,20 @@ static int64_t batch_extent(int64_t e, int64_t s, int64_t batch)
     return (int64_t)t;
 }
 
-static int sgemm_call(const Call &c, cudaStream_t stream)
+// Status of validate_call() for a call with no output entries (not exported).
+constexpr int kNothingToDo = -1;
+
+// Argument checks of a general-form call: SGEMM_OK, kNothingToDo (no output
+// entries), or the status code the call returns. Null pointers and C
+// overlapping A or B are checked only with `pointers` set: the plan takes
+// operand addresses for their alignment alone.
+static int validate_call(const Call &c, bool pointers)
 {
     if (c.config < -1 || c.config >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
     if ((c.op_a != 0 && c.op_a != 1) || (c.op_b != 0 && c.op_b != 1)) return SGEMM_ERR_INVALID_VALUE;
     if (c.M < 0 || c.N < 0 || c.K < 0 || c.batch < 0) return SGEMM_ERR_INVALID_VALUE;
     if (c.sa < 0 || c.sb < 0 || c.sc < 0) return SGEMM_ERR_INVALID_VALUE;
-    if (c.batch == 0 || c.M == 0 || c.N == 0) return SGEMM_OK;
+    if (c.batch == 0 || c.M == 0 || c.N == 0) return kNothingToDo;
     // Stored shapes: A is M x K (op 0) or K x M (op 1); B is K x N or N x K.
     const int64_t a_rows = c.op_a ? c.K : c.M, a_cols = c.op_a ? c.M : c.K;
     const int64_t b_rows = c.op_b ? c.N : c.K, b_cols = c.op_b ? c.K : c.N;
@@ -239,33 +246,29 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     if (c.batch > 1 && c.sc < c_one) return SGEMM_ERR_INVALID_VALUE;   // C entries must not overlap
     const int64_t c_all = batch_extent(c_one, c.sc, c.batch);
     if (c_all < 0) return SGEMM_ERR_OVERFLOW;
-    if (c.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
-    const uint64_t a = (uint64_t)(uintptr_t)c.A, b = (uint64_t)(uintptr_t)c.B, cp = (uint64_t)(uintptr_t)c.C;
-    int64_t a_all = 0, b_all = 0;
+    if (pointers && c.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
     if (reads_ab) {
-        if (c.A == nullptr || c.B == nullptr) return SGEMM_ERR_INVALID_VALUE;
+        if (pointers && (c.A == nullptr || c.B == nullptr)) return SGEMM_ERR_INVALID_VALUE;
         const int64_t a_one = extent(a_rows, a_cols, c.lda), b_one = extent(b_rows, b_cols, c.ldb);
         if (a_one < 0 || b_one < 0) return SGEMM_ERR_OVERFLOW;
-        a_all = batch_extent(a_one, c.sa, c.batch);
-        b_all = batch_extent(b_one, c.sb, c.batch);
+        const int64_t a_all = batch_extent(a_one, c.sa, c.batch);
+        const int64_t b_all = batch_extent(b_one, c.sb, c.batch);
         if (a_all < 0 || b_all < 0) return SGEMM_ERR_OVERFLOW;
-        if (overlaps(cp, c_all, a, a_all) || overlaps(cp, c_all, b, b_all)) return SGEMM_ERR_INVALID_VALUE;
+        const uint64_t a = (uint64_t)(uintptr_t)c.A, b = (uint64_t)(uintptr_t)c.B, cp = (uint64_t)(uintptr_t)c.C;
+        if (pointers && (overlaps(cp, c_all, a, a_all) || overlaps(cp, c_all, b, b_all)))
+            return SGEMM_ERR_INVALID_VALUE;
     }
+    return SGEMM_OK;
+}
+
+// The configuration of a validated call that reads A and B (K > 0, alpha
+// != 0), automatic or forced, and whether A and B go through scratch first.
+// Returns SGEMM_OK or SGEMM_ERR_UNSUPPORTED.
+static int plan_call(const Call &c, int num_sms, int *out_cfg, bool *out_pa, bool *out_pb)
+{
+    const uint64_t a = (uint64_t)(uintptr_t)c.A, b = (uint64_t)(uintptr_t)c.B, cp = (uint64_t)(uintptr_t)c.C;
     const bool plain = c.op_a == 0 && c.op_b == 0 && c.alpha == 1.0f && c.beta == 0.0f && c.batch == 1;
-
-    DeviceState *dev = nullptr;
-    int rc = device_state(&dev);
-    if (rc != SGEMM_OK) return rc;
-
-    if (!reads_ab) {
-        // The empty sum (K == 0) or alpha == 0: C = beta * C.
-        if (c.beta == 1.0f) return SGEMM_OK;
-        return launch_scale(c.C, c.M, c.N, c.ldc, c.sc, c.batch, c.beta, stream) == cudaSuccess
-                   ? SGEMM_OK
-                   : SGEMM_ERR_LAUNCH;
-    }
-
-    const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, dev->num_sms};
+    const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, num_sms};
     int cfg = c.config < 0 ? select_config(p) : c.config;
     // The automatic choice for tiny products is a plain-form-only kernel of
     // the pages' ladder; the general form takes the smallest TMA tiles instead.
@@ -278,6 +281,47 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     if (!config_supports(cfg, p)) return SGEMM_ERR_UNSUPPORTED;
     // Kernels without TMA (the simple and ladder kernels) run the plain form only.
     if (!plain && !kConfigTable[cfg].uses_tma) return SGEMM_ERR_UNSUPPORTED;
+    // TMA FFMA configurations read A (M x K) and B (K x N) in place when the
+    // rows and batch strides are 16-byte multiples on a 16-byte-aligned base;
+    // anything else (a transposed operand included) is packed into scratch,
+    // rows padded to 32 floats. A shared operand (batch stride 0) is packed once.
+    // A k-major configuration takes A stored K x M instead: in place when the
+    // caller stores it so (op_a 1) on those terms, else transposed (a plain
+    // A) or copied (a misaligned transposed one) into scratch.
+    const bool packs = kConfigTable[cfg].packs;
+    const bool akm = kConfigTable[cfg].a_kmajor;
+    auto stride_ok = [&](int64_t s, int64_t one) { return c.batch <= 1 || s == 0 || (s % 4 == 0 && s >= one); };
+    *out_pa = packs && (akm ? (c.op_a == 0 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.K * c.lda))
+                            : (c.op_a == 1 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.M * c.lda)));
+    *out_pb = packs && (c.op_b == 1 || needs_pack(b, c.ldb) || !stride_ok(c.sb, c.K * c.ldb));
+    *out_cfg = cfg;
+    return SGEMM_OK;
+}
+
+static int sgemm_call(const Call &c, cudaStream_t stream)
+{
+    int rc = validate_call(c, true);
+    if (rc == kNothingToDo) return SGEMM_OK;
+    if (rc != SGEMM_OK) return rc;
+    const bool reads_ab = c.K > 0 && c.alpha != 0.0f;
+    const int64_t a_rows = c.op_a ? c.K : c.M, a_cols = c.op_a ? c.M : c.K;
+
+    DeviceState *dev = nullptr;
+    rc = device_state(&dev);
+    if (rc != SGEMM_OK) return rc;
+
+    if (!reads_ab) {
+        // The empty sum (K == 0) or alpha == 0: C = beta * C.
+        if (c.beta == 1.0f) return SGEMM_OK;
+        return launch_scale(c.C, c.M, c.N, c.ldc, c.sc, c.batch, c.beta, stream) == cudaSuccess
+                   ? SGEMM_OK
+                   : SGEMM_ERR_LAUNCH;
+    }
+
+    int cfg = -1;
+    bool pa = false, pb = false;
+    rc = plan_call(c, dev->num_sms, &cfg, &pa, &pb);
+    if (rc != SGEMM_OK) return rc;
 
     GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
     g.sched = c.sched_override >= 0 ? c.sched_override : kConfigTable[cfg].sched;
@@ -292,19 +336,7 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     g.op_a = c.op_a;
     g.op_b = c.op_b;
 
-    // TMA FFMA configurations read A (M x K) and B (K x N) in place when the
-    // rows and batch strides are 16-byte multiples on a 16-byte-aligned base;
-    // anything else (a transposed operand included) is packed into scratch,
-    // rows padded to 32 floats. A shared operand (batch stride 0) is packed once.
-    // A k-major configuration takes A stored K x M instead: in place when the
-    // caller stores it so (op_a 1) on those terms, else transposed (a plain
-    // A) or copied (a misaligned transposed one) into scratch.
-    const bool packs = kConfigTable[cfg].packs;
     const bool akm = kConfigTable[cfg].a_kmajor;
-    auto stride_ok = [&](int64_t s, int64_t one) { return c.batch <= 1 || s == 0 || (s % 4 == 0 && s >= one); };
-    const bool pa = packs && (akm ? (c.op_a == 0 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.K * c.lda))
-                                  : (c.op_a == 1 || needs_pack(a, c.lda) || !stride_ok(c.sa, c.M * c.lda)));
-    const bool pb = packs && (c.op_b == 1 || needs_pack(b, c.ldb) || !stride_ok(c.sb, c.K * c.ldb));
     const int64_t a_rows_p = akm ? c.K : c.M;                       // rows of the packed A
     const int64_t lda_p = round_up(akm ? c.M : c.K, 32), ldb_p = round_up(c.N, 32);
     const int64_t a_entries = (c.batch > 1 && c.sa != 0) ? c.batch : 1;
@@ -478,6 +510,33 @@ int sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alp
 {
     return sgemm_general_ex(op_a, op_b, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
                             stride_c, batch, -1, stream);
+}
+
+int sgemm_general_plan(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha, int64_t lda,
+                       int64_t stride_a, int64_t ldb, int64_t stride_b, float beta, int64_t ldc, int64_t stride_c,
+                       int64_t batch, uint64_t a_addr, uint64_t b_addr, uint64_t c_addr, int num_sms, int config,
+                       int *out_config, int *out_pack_a, int *out_pack_b)
+{
+    if (out_config) *out_config = -1;
+    if (out_pack_a) *out_pack_a = 0;
+    if (out_pack_b) *out_pack_b = 0;
+    if (num_sms <= 0) return SGEMM_ERR_INVALID_VALUE;
+    const Call c{op_a, op_b, M, N, K, alpha,
+                 reinterpret_cast<const float *>((uintptr_t)a_addr), lda, stride_a,
+                 reinterpret_cast<const float *>((uintptr_t)b_addr), ldb, stride_b, beta,
+                 reinterpret_cast<float *>((uintptr_t)c_addr), ldc, stride_c, batch, config, -1, -1};
+    int rc = validate_call(c, false);
+    if (rc == kNothingToDo) return SGEMM_OK;
+    if (rc != SGEMM_OK) return rc;
+    if (K == 0 || alpha == 0.0f) return SGEMM_OK;   // no product: C = beta * C only
+    int cfg = -1;
+    bool pa = false, pb = false;
+    rc = plan_call(c, num_sms, &cfg, &pa, &pb);
+    if (rc != SGEMM_OK) return rc;
+    if (out_config) *out_config = cfg;
+    if (out_pack_a) *out_pack_a = pa ? 1 : 0;
+    if (out_pack_b) *out_pack_b = pb ? 1 : 0;
+    return SGEMM_OK;
 }
 
 int sgemm_check_status(cudaStream_t stream)

@@ -180,6 +180,34 @@ int sgemm_general_ex(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float 
                      int64_t batch, int config, cudaStream_t stream);
 
 /*
+ * sgemm_general_plan — host-only view of the choice sgemm_general_ex() makes
+ * (the pages have no counterpart); needs no GPU.
+ *
+ *   op_a ... batch           as sgemm_general_ex(), with the operands given
+ *                            by address (only their alignment matters; 0
+ *                            means aligned; null and overlap are not checked).
+ *   num_sms                  streaming multiprocessors of the target device.
+ *   config                   -1 (automatic) or a forced configuration.
+ *   out_config               (nullable) receives the configuration of the
+ *                            product, or -1 when the call runs none (no
+ *                            output entries, or K == 0 or alpha == 0, which
+ *                            only scale C).
+ *   out_pack_a, out_pack_b   (nullable) receive 1 if that operand goes
+ *                            through scratch first (packed, transposed or,
+ *                            for A under a k-major configuration, transposed
+ *                            to K x M), else 0.
+ *
+ * Returns SGEMM_OK, or the code sgemm_general_ex() would return for these
+ * sizes, strides and configuration.
+ */
+int sgemm_general_plan(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                       int64_t lda, int64_t stride_a, int64_t ldb, int64_t stride_b,
+                       float beta, int64_t ldc, int64_t stride_c, int64_t batch,
+                       uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+                       int num_sms, int config,
+                       int *out_config, int *out_pack_a, int *out_pack_b);
+
+/*
  * sgemm_check_status — waits for `stream`, then reads and clears the current
  * device's error word. Returns SGEMM_ERR_TIMEOUT if any kernel of this
  * library on the device gave up a bounded wait since the last check (its

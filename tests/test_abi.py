@@ -135,3 +135,30 @@ def test_fail_next_allocs_hook_validates_its_count():
     assert sg.sgemm_test_fail_next_allocs(-1) == sg.SGEMM_ERR_INVALID_VALUE
     assert sg.sgemm_test_fail_next_allocs(2) == sg.SGEMM_OK
     assert sg.sgemm_test_fail_next_allocs(0) == sg.SGEMM_OK
+
+
+def test_general_plan_follows_the_library_choice():
+    name = lambda c: sg.sgemm_config_name(c) if c >= 0 else None
+    plan = lambda *a, config=-1: sg.sgemm_general_plan(*a, 0, 0, 0, 152, config)
+    # A transposed A (K x M, aligned) is read in place by the k-major configuration...
+    rc, cfg, pa, pb = plan(1, 0, 4096, 4096, 4096, 1.0, 4096, 0, 4096, 0, 0.0, 4096, 0, 1)
+    assert (rc, name(cfg), pa, pb) == (0, "ffma2_128x256_k32_s4_ka", 0, 0)
+    # ...a plain A is transposed for it, and a transposed B is packed.
+    rc, cfg, pa, pb = plan(0, 1, 4096, 4096, 4096, 1.0, 4096, 0, 4096, 0, 0.0, 4096, 0, 1)
+    assert (rc, name(cfg), pa, pb) == (0, "ffma2_128x256_k32_s4_ka", 1, 1)
+    # A transposed A on rows that are not a multiple of 4 floats is copied first.
+    rc, cfg, pa, pb = plan(1, 0, 4096, 4096, 4096, 1.0, 4097, 0, 4096, 0, 0.0, 4096, 0, 1)
+    assert (rc, pa, pb) == (0, 1, 0)
+    # Below N = 2048 the row-major configuration reads an aligned strided batch in place.
+    rc, cfg, pa, pb = plan(0, 0, 1024, 1024, 1024, 1.0, 1024, 1 << 20, 1024, 0, 0.0, 1024, 1 << 20, 16)
+    assert (rc, name(cfg), pa, pb) == (0, "ffma2_128x128_k32_s4", 0, 0)
+    # Tiny general products take the smallest TMA tiles, not the pages' ladder kernel.
+    rc, cfg, pa, pb = plan(0, 0, 150, 200, 70, -1.5, 73, 150 * 73, 205, 70 * 205, 2.0, 202, 150 * 202, 3)
+    assert (rc, name(cfg), pa, pb) == (0, "ffma2_128x64_k32_s4", 1, 1)
+    # K == 0 only scales C: no product configuration.
+    assert plan(0, 0, 150, 200, 0, 1.0, 1, 0, 200, 0, 2.0, 202, 0, 1)[:2] == (0, -1)
+    # Status codes as sgemm_general_ex(): overlapping C entries, a plain-form-only forced configuration.
+    assert plan(0, 0, 150, 200, 70, 1.0, 70, 0, 200, 0, 0.0, 202, 0, 3)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    ladder = sg.config_ids()["ladder_register_tiled_2x2"]
+    assert plan(0, 0, 256, 256, 256, 1.0, 256, 0, 256, 0, 0.5, 256, 0, 1, config=ladder)[0] == \
+        sg.SGEMM_ERR_UNSUPPORTED
