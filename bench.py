@@ -575,9 +575,13 @@ def main():
         rc, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(),
                                         dB.data_ptr(), dC.data_ptr(), num_sms)
         if args.noalloc and sg.sgemm_config_name(cfg).endswith("_ka"):
-            # sgemm_noalloc runs the twin that reads A as stored (no scratch for A).
-            cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
-            pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
+            # sgemm_noalloc makes the transposed copy of A in its fixed 16 Mi-float
+            # array when it fits beside a packed B, else runs the twin that reads A
+            # as stored.
+            r32 = lambda x: (x + 31) // 32 * 32
+            if w.K * r32(w.M) + (w.K * r32(w.N) if pb else 0) > (16 << 20):
+                cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
+                pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
         launches_per_step = 1 + pa + pb
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
         flops = product_flops(w.M, w.N, w.K)

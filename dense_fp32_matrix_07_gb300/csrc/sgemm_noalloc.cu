@@ -18,8 +18,9 @@
 // 152 SMs); a schedule that would need more runs whole tiles instead.
 //
 // Where sgemm() would take a k-major configuration (one that reads A as a
-// transposed copy, which needs scratch for the whole of A), this entry point
-// runs that configuration's twin, which reads A as stored.
+// transposed copy), this entry point makes that copy in its fixed array when
+// it fits there (K * round_up(M, 32) floats, beside a packed B), and
+// otherwise runs the configuration's twin, which reads A as stored.
 //
 // Sharing: every call on a device uses the same arrays, which keep whatever
 // the last call left in them. Nothing in it has to start at zero (each call
@@ -172,15 +173,18 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     int cfg = -1, pack_a = 0, pack_b = 0;
     rc = sgemm_plan(M, N, K, lda, ldb, ldc, a, b, c, dev->num_sms, &cfg, &pack_a, &pack_b);
     if (rc != SGEMM_OK) return rc;
-    // A configuration that takes A k-major would need scratch for the whole
-    // transposed A; this entry point runs its twin that reads A as stored.
-    if (kConfigTable[cfg].a_kmajor) {
+    // A configuration that takes A k-major reads a transposed copy of A
+    // (K rows of round_up(M, 32) floats): made in the fixed array when it fits
+    // there beside a packed B, else the twin that reads A as stored runs.
+    const int64_t ldb_p = round_up32(N);
+    const int64_t b_floats = pack_b ? K * ldb_p : 0;
+    const bool a_kmajor = kConfigTable[cfg].a_kmajor && K * round_up32(M) + b_floats <= kNoAllocScratchFloats;
+    if (kConfigTable[cfg].a_kmajor && !a_kmajor) {
         cfg = cfg == kCfgFfma2_128x128_ka ? kCfgFfma2_128x128 : kCfgFfma2_128x256;
         pack_a = ((a & 15u) != 0 || lda % 4 != 0) ? 1 : 0;
     }
-    const int64_t lda_p = round_up32(K), ldb_p = round_up32(N);
-    const int64_t a_floats = pack_a ? M * lda_p : 0;
-    const int64_t b_floats = pack_b ? K * ldb_p : 0;
+    const int64_t lda_p = a_kmajor ? round_up32(M) : round_up32(K);
+    const int64_t a_floats = pack_a ? (a_kmajor ? K : M) * lda_p : 0;
     if (a_floats > kNoAllocScratchFloats || b_floats > kNoAllocScratchFloats ||
         a_floats + b_floats > kNoAllocScratchFloats)
         return SGEMM_ERR_SCRATCH_LIMIT;
@@ -197,7 +201,15 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     } else {
         g.sched = kSchedDataParallel;
     }
-    if (pack_a) {
+    if (a_kmajor) {
+        // The transposed copy, K x M with rows of lda_p floats.
+        if (launch_pack_transpose_batched(A, M, K, lda, 0, dev->scratch, lda_p, K * lda_p, 1, stream) !=
+            cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        g.A = dev->scratch;
+        g.lda = lda_p;
+        g.op_a = 1;
+    } else if (pack_a) {
         if (pack_into_scratch(A, M, K, lda, 0, lda_p, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         g.A = dev->scratch;
         g.lda = lda_p;

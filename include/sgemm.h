@@ -338,9 +338,10 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
  * such operands into a fixed scratch array compiled into the library instead,
  * keeps the stream-K partial sums and flags in a second fixed array (24 MiB;
  * a schedule needing more, on GPUs of over 190 SMs, runs whole tiles), and
- * allocates nothing. Where sgemm() would take a k-major configuration, which
- * needs scratch for the whole transposed A, this entry point runs that
- * configuration's twin that reads A as stored.
+ * allocates nothing. Where sgemm() would take a k-major configuration, this
+ * entry point makes its transposed copy of A in the fixed array when that
+ * fits (K * round_up(M, 32) floats, beside a packed B), and otherwise runs
+ * the configuration's twin that reads A as stored.
  *
  * Arguments, semantics, ownership and status codes: as sgemm().
  *
