@@ -398,7 +398,8 @@ FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_reg
               "sgemm_inner_loop_8x16_smem_column_serpentine_reversed_odd_k",
               "sgemm_inner_loop_8x16_smem_kmajor_a_column_serpentine", "sgemm_inner_loop_8x16_smem_kmajor_a",
               "sgemm_inner_loop_8x8_smem_kmajor_a_column_serpentine",
-              "sgemm_inner_loop_8x16_smem_kmajor_a_column_serpentine_setmaxnreg_384")
+              "sgemm_inner_loop_8x16_smem_kmajor_a_column_serpentine_setmaxnreg_384",
+              "sgemm_inner_loop_8x16_smem_scalar_a_column_serpentine", "sgemm_inner_loop_8x16_smem_scalar_a")
 
 
 def run_fma_probe():

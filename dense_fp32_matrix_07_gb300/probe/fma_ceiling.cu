@@ -47,6 +47,9 @@
 //      serpentine
 //  27  as 24 in the main kernel's launch shape: 384 threads, the third
 //      warpgroup leaving after setmaxnreg hands 232 registers to the others
+//  28  as 18 (row-major A slab, column serpentine), the 8 A values of one
+//      k read by 8 scalar shared loads in place of 4-k LDS.128 per row
+//  29  as 28, row-major order
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -281,7 +284,7 @@ namespace {
 // at chunk c ^ (r & 7); B is [32][BN] floats. Each thread loads 4 k of A per
 // row with one LDS.128 and TN/4 float4 of B per k, then issues TM * TN / 2
 // broadcast FFMA2 per k.
-template <int TN, int WM = 2, bool SWAP = false, int ORDER = -1>
+template <int TN, int WM = 2, bool SWAP = false, int ORDER = -1, bool SCALAR_A = false>
 __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int iters, unsigned long long *clk)
 {
     constexpr int TM = 8, TR = 8, TC = 4, WN = 4;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
         for (int kb = 0; kb < 8; ++kb) {
             float a[TM][4];
 #pragma unroll
-            for (int i = 0; i < TM; ++i) {
+            for (int i = 0; i < TM && !SCALAR_A; ++i) {
                 const int r = ty + TR * i;    // (wm + r) & 7 == r & 7
                 const float4 v =
                     *reinterpret_cast<const float4 *>(Ai + TR * i * 128 + (((unsigned)kb ^ (unsigned)(r & 7)) << 4));
@@ -333,8 +336,21 @@ __global__ void __launch_bounds__(WM * 4 * 32, 1) inner_kernel(float *out, int i
                 if constexpr (ORDER >= 0) {
                     float ak[TM];
                     float2 b2[TN / 2];
+                    if constexpr (SCALAR_A) {
+                        // One 4-byte shared load per row at this k: row
+                        // ty + 8i, 16-byte chunk kb ^ ty, word kk. The 8 rows
+                        // of a warp's distinct ty fall in 8 distinct chunks,
+                        // so the loads are conflict-free; inline PTX keeps
+                        // them from being merged into the 16-byte loads.
+                        const unsigned base = (unsigned)__cvta_generic_to_shared(Ai) +
+                                              ((((unsigned)kb ^ (unsigned)(ty & 7)) << 4) | (unsigned)(kk * 4));
 #pragma unroll
-                    for (int i = 0; i < TM; ++i) ak[i] = a[i][kk];
+                        for (int i = 0; i < TM; ++i)
+                            asm("ld.shared.f32 %0, [%1];" : "=f"(ak[i]) : "r"(base + (unsigned)(TR * i * 128)));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < TM; ++i) ak[i] = a[i][kk];
+                    }
 #pragma unroll
                     for (int g = 0; g < TN / 4; ++g) {
                         b2[2 * g] = make_float2(b[g].x, b[g].y);
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__(SPLIT ? 384 : 256, 1) inner_kmajor_kernel(floa
 extern "C" {
 
 // Number of probe kinds (see the list at the top of this file).
-int fma_probe_count(void) { return 28; }
+int fma_probe_count(void) { return 30; }
 
 // Runs probe `kind` on one block per SM: one warm-up launch, then `reps`
 // timed launches (CUDA events); returns the best launch time, the SM clock
@@ -458,7 +474,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (kind < 0 || kind > 27 || reps < 1) return (int)cudaErrorInvalidValue;
+    if (kind < 0 || kind > 29 || reps < 1) return (int)cudaErrorInvalidValue;
     float *out = nullptr;
     unsigned long long *clk = nullptr;
     if ((e = cudaMalloc(&out, sizeof(float) * 384 * (size_t)sms)) != cudaSuccess) return (int)e;
@@ -497,6 +513,8 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
         case 25: inner_kmajor_kernel<0><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         case 26: inner_kmajor_kernel<2, 8><<<sms, 256, inner_smem<8>()>>>(out, loop_iters, clk); break;
         case 27: inner_kmajor_kernel<2, 16, true><<<sms, 384, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 28: inner_kernel<16, 2, false, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
+        case 29: inner_kernel<16, 2, false, 0, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         default: inner_kernel<16, 2, true><<<sms, 256, inner_smem<16>()>>>(out, loop_iters, clk); break;
         }
     };
@@ -504,7 +522,7 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
     else if (kind <= 4 || kind == 8 || (kind >= 10 && kind <= 13)) f = 2.0 * 64 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind >= 14 && kind <= 16) f = 2.0 * 128 * 32 * (double)loop_iters * 256.0 * sms;
     else if (kind == 5 || kind == 19 || kind == 20 || kind == 26) f = 2.0 * 128 * 128 * 32 * (double)loop_iters * sms;
-    else if (kind == 6 || kind == 9 || (kind >= 17 && kind <= 25) || kind == 27) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
+    else if (kind == 6 || kind == 9 || (kind >= 17 && kind <= 25) || kind >= 27) f = 2.0 * 128 * 256 * 32 * (double)loop_iters * sms;
     else f = 2.0 * 192 * 128 * 32 * (double)loop_iters * sms;
     e = cudaFuncSetAttribute(inner_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, inner_smem<8>());
     if (e == cudaSuccess)
@@ -538,6 +556,12 @@ int fma_probe_run(int kind, int reps, double *best_ms, double *sm_mhz, double *f
                                  inner_smem<16>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inner_kmajor_kernel<2, 16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 inner_smem<16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inner_kernel<16, 2, false, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  inner_smem<16>());
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
