@@ -184,7 +184,7 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         pack_a = ((a & 15u) != 0 || lda % 4 != 0) ? 1 : 0;
     }
     const int64_t lda_p = a_kmajor ? round_up32(M) : round_up32(K);
-    const int64_t a_floats = pack_a ? (a_kmajor ? K : M) * lda_p : 0;
+    const int64_t a_floats = a_kmajor ? K * lda_p : (pack_a ? M * lda_p : 0);
     if (a_floats > kNoAllocScratchFloats || b_floats > kNoAllocScratchFloats ||
         a_floats + b_floats > kNoAllocScratchFloats)
         return SGEMM_ERR_SCRATCH_LIMIT;
