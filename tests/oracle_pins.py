@@ -42,7 +42,7 @@ def _pair(M, N, K, dist, seed):
     return A.numpy(), B.numpy()
 
 
-def check_bruteforce_rational(o, max_dim=5, seed=11):
+def check_bruteforce_rational(o, max_dim=6, seed=11):
     """All M, N, K in 1..max_dim: exact rational sum of exact products."""
     rng = np.random.default_rng(seed)
     for M, N, K in itertools.product(range(1, max_dim + 1), repeat=3):
