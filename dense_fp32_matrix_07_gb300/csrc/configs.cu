@@ -65,11 +65,17 @@ int select_config(const ProblemShape &p)
     // 1300 (same-box sweep: 4096^3 86.3 % against 84.3 % of the FP32 peak,
     // 16384^3 87.8 % against 85.2 %, 2048^3 forced onto 128x256 tiles 80.0 %
     // against 79.4 %).
-    if (tiles256 >= p.num_sms) return p.N >= 2048 ? kCfgFfma2_128x256_ka : kCfgFfma2_128x256;
+    // The pass also costs about 5 us whatever its size (a launch and its
+    // drain), which the faster loop, about 2.5 % of the product, repays once
+    // the product takes about 200 us: M*N*K >= 6e9 (same-box sweep, row-major
+    // against k-major: 2048 x 2048 x 512 81.6 against 85.7 us, 1536 x 2048 x
+    // 2048 212.6 against 212.7 us, 2048^3 276.1 against 274.1 us).
+    const bool kmajor = p.N >= 2048 && (double)p.M * (double)p.N * (double)p.K >= 6.0e9;
+    if (tiles256 >= p.num_sms) return kmajor ? kCfgFfma2_128x256_ka : kCfgFfma2_128x256;
     // The 128x128 block's k-major twin by the same rule (8x8 loop alone 89.5 %
     // against 86.0 %; same-box sweep: 2048^3 78.3 % against 77.3 %, 2048 x
     // 2048 x 8192 84.0 % against 81.0 %, but 1024^3 50.7 % against 54.2 %).
-    if (3 * tiles128 >= p.num_sms) return p.N >= 2048 ? kCfgFfma2_128x128_ka : kCfgFfma2_128x128;
+    if (3 * tiles128 >= p.num_sms) return kmajor ? kCfgFfma2_128x128_ka : kCfgFfma2_128x128;
     return kCfgFfma2_128x64;
 }
 

@@ -108,6 +108,17 @@ def test_plan_tile_size_follows_the_problem(n, name):
     assert rc == 0 and sg.sgemm_config_name(cfg) == name
 
 
+@pytest.mark.parametrize("M,N,K,name", [
+    (2048, 2048, 512, "ffma2_128x128_k32_s4"),      # M*N*K = 2.1e9: the transpose pass would not pay
+    (4096, 4096, 256, "ffma2_128x256_k32_s4"),      # 4.3e9: the same on 128x256 tiles
+    (1536, 2048, 2048, "ffma2_128x128_k32_s4_ka"),  # 6.4e9 and N >= 2048: A k-major
+    (4096, 1536, 4096, "ffma2_128x256_k32_s4"),     # N < 2048 at any size: A read as stored
+])
+def test_plan_takes_the_kmajor_pass_only_when_it_pays(M, N, K, name):
+    rc, cfg, pa, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, 152)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == name and pa == (1 if name.endswith("_ka") else 0)
+
+
 def test_plan_long_k_skips_the_simple_kernel():
     # A tiny output with a long K goes to the stream-K kernel, not one small block.
     rc, cfg, *_ = sg.sgemm_plan(1, 1, 1 << 20, 1 << 20, 1, 1, 0, 0, 0, 148)

@@ -74,10 +74,11 @@ def test_cluster_kernel_refuses_a_launch_without_its_cluster(cuda_device, oracle
 
 
 def test_kmajor_choice_falls_back_when_its_scratch_cannot_be_had(cuda_device, oracle):
-    # N >= 2048 and enough 128x128 tiles: the automatic choice is a k-major
-    # configuration, which needs scratch for the transposed A. With that
-    # allocation failing, the row-major twin runs the product instead.
-    M, N, K = 512, 2048, 256
+    # N >= 2048, M*N*K >= 6e9 and enough 128x128 tiles: the automatic choice
+    # is a k-major configuration, which needs scratch for the transposed A.
+    # With that allocation failing, the row-major twin runs the product
+    # instead.
+    M, N, K = 1024, 2048, 2944
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rc, cfg, pa, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, sms)
     assert rc == 0 and sg.sgemm_config_name(cfg).endswith("_ka") and pa == 1

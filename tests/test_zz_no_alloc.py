@@ -64,14 +64,14 @@ def test_noalloc_matches_sgemm_on_two_calls_in_a_row(cuda_device, oracle, case):
         assert_parity(c_new, Cref, S, dist == "int", f"noalloc call {call}")
 
 
-@pytest.mark.parametrize("shape", [(1024, 2048, 512), (8192, 2048, 2052)], ids=["kmajor_copy", "twin"])
+@pytest.mark.parametrize("shape", [(1024, 2048, 2944), (8192, 2048, 2052)], ids=["kmajor_copy", "twin"])
 def test_noalloc_kmajor_choice(cuda_device, oracle, shape):
-    # N >= 2048: sgemm() takes a k-major configuration and transposes A into
-    # pool scratch. sgemm_noalloc() makes that copy in its fixed array when
-    # it fits (1024 x 2048 x 512: 512 x 1024 floats), else runs the twin that
-    # reads A as stored (8192 x 2048 x 2052: the copy would be 2052 x 8192
-    # floats, over 16 Mi, while A's rows, 2052 floats, need no pack). Integer
-    # inputs: both give the exact product.
+    # N >= 2048 and M*N*K >= 6e9: sgemm() takes a k-major configuration and
+    # transposes A into pool scratch. sgemm_noalloc() makes that copy in its
+    # fixed array when it fits (1024 x 2048 x 2944: 2944 x 1024 floats), else
+    # runs the twin that reads A as stored (8192 x 2048 x 2052: the copy
+    # would be 2052 x 8192 floats, over 16 Mi, while A's rows, 2052 floats,
+    # need no pack). Integer inputs: both give the exact product.
     M, N, K = shape
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rc, cfg, pa, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, sms)
