@@ -98,11 +98,12 @@ enum {
  * whose base address is 16-byte aligned and whose leading dimension is a
  * multiple of 4 floats are read in place by the tensor-memory-accelerator
  * (TMA) path; others are first packed into aligned scratch. For products of
- * 128x256 or 128x128 tiles with N >= 2048 the automatic choice is a k-major
- * configuration ("ffma2_128x256_k32_s4_ka", "ffma2_128x128_k32_s4_ka"),
- * whose kernel reads A as a K x M matrix: A is first transposed into
- * scratch (K * round_up(M, 32) floats, about 8*M*K bytes of traffic), which
- * its faster inner loop repays. C is written with 16-byte vector stores when
+ * 128x256 or 128x128 tiles with N >= 2048 and M*N*K >= 6e9 the automatic
+ * choice is a k-major configuration ("ffma2_128x256_k32_s4_ka",
+ * "ffma2_128x128_k32_s4_ka"), whose kernel reads A as a K x M matrix: A is
+ * first transposed into scratch (K * round_up(M, 32) floats, about 8*M*K
+ * bytes of traffic and a fixed few microseconds), which its faster inner
+ * loop repays at those sizes. C is written with 16-byte vector stores when
  * it is aligned the same way, else with scalar stores.
  *
  * Returns SGEMM_OK or one of the codes above. A device-side timeout cannot
