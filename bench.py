@@ -500,6 +500,65 @@ def run_shape_sweep(shapes, config):
     return 0
 
 
+def run_config_comparison(shapes, names):
+    """Times each named configuration, forced, on each "MxNxK" shape (tight
+    strides, N(0,1) inputs drawn on the device from seed 0): a 256 MB write
+    between calls, so every call starts with a cold L2, and the median of up
+    to 100 calls or 0.5 s per configuration. One JSON line per shape, for
+    selector studies, not a bench line."""
+    import torch
+    import dense_fp32_matrix_07_gb300 as sg
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    unknown = [n for n in names if n not in ids]
+    if unknown:
+        raise SystemExit(f"unknown configurations: {unknown}")
+    scrub = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    for shp in shapes:
+        M, N, K = (int(x) for x in shp.lower().split("x"))
+        g = torch.Generator(device=dev).manual_seed(0)
+        A = torch.randn(M, K, device=dev, generator=g)
+        B = torch.randn(K, N, device=dev, generator=g)
+        C = torch.empty(M, N, device=dev)
+        rc, auto_cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(), C.data_ptr(), sms)
+        times = {}
+        for name in names:
+            cfg = ids[name]
+
+            def call():
+                return sg.sgemm_ex(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, cfg, sh)
+
+            if call() != 0:
+                times[name] = None
+                continue
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            ts = []
+            for r in range(100):
+                scrub.fill_(float(r))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+                if sum(ts) > 500.0:
+                    break
+            rc = sg.sgemm_check_status(sh)
+            if rc != 0:
+                raise RuntimeError(f"{shp} {name}: {sg.sgemm_error_string(rc)}")
+            ts.sort()
+            times[name] = round(ts[len(ts) // 2] * 1e3, 1)
+        print(json.dumps({"compare": "configs", "shape": shp, "auto": sg.sgemm_config_name(auto_cfg),
+                          "median_us": times}), flush=True)
+        del A, B, C
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,6 +587,9 @@ def main():
                     help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
     ap.add_argument("--shapes", default="", metavar="MxNxK[,MxNxK...]",
                     help="time the product on these shapes back to back (automatic or --config) and exit")
+    ap.add_argument("--compare-configs", default="", metavar="NAME[,NAME...]",
+                    help="with --shapes: time each named configuration, forced, on every shape (cold L2, "
+                         "medians) and exit")
     ap.add_argument("--probe-l2", type=int, default=0, metavar="MIB",
                     help="every SM reads the same MIB-MiB buffer (L2 sharing probe, for ncu) and exit")
     args = ap.parse_args()
@@ -541,6 +603,9 @@ def main():
         return run_fma_probe()
     if args.probe_l2:
         return run_l2_probe(args.probe_l2)
+    if args.shapes and args.compare_configs:
+        return run_config_comparison([x for x in args.shapes.split(",") if x],
+                                     [x for x in args.compare_configs.split(",") if x])
     if args.shapes:
         return run_shape_sweep([x for x in args.shapes.split(",") if x], args.config)
 
