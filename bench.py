@@ -506,16 +506,17 @@ def run_config_comparison(shapes, names):
     between calls, so every call starts with a cold L2, and the median of up
     to 100 calls or 0.5 s per configuration. One JSON line per shape, for
     selector studies, not a bench line."""
-    import torch
     import dense_fp32_matrix_07_gb300 as sg
+    # Names are checked on the host before any device work.
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    unknown = [n for n in names if n not in ids]
+    if unknown or not names:
+        raise SystemExit(f"unknown configurations: {unknown} (known: {sorted(ids)})")
+    import torch
     dev = torch.device("cuda", 0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
-    unknown = [n for n in names if n not in ids]
-    if unknown:
-        raise SystemExit(f"unknown configurations: {unknown}")
     scrub = torch.empty(64 << 20, dtype=torch.float32, device=dev)
     for shp in shapes:
         M, N, K = (int(x) for x in shp.lower().split("x"))

@@ -7,6 +7,7 @@ import json
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 import torch
@@ -119,3 +120,12 @@ def test_profiled_traffic_is_reported_only_for_the_profiled_kernel():
     else:
         assert bench.profiled_traffic(cfg) is None     # stale summary: no traffic claim
     assert bench.profiled_traffic("some_other_config") is None
+
+
+def test_config_comparison_rejects_unknown_names_before_any_device_work():
+    # Runs on a host without a GPU: the names are checked first.
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--shapes", "64x64x64",
+                        "--compare-configs", "ffma2_128x256_k32_s4_ka,no_such_config"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode != 0
+    assert "no_such_config" in r.stderr and "ffma2_128x256_k32_s4_ka" in r.stderr
