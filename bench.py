@@ -1,15 +1,16 @@
 """SGEMM throughput bench (GFLOP/s and % of the GB300 FP32 FFMA peak).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload NAME] [--config ID]
+python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME | --shape MxNxK] [--config ID]
                 [--op-a 0|1] [--op-b 0|1] [--alpha X] [--beta Y] [--batch B]
+                [--extra-workloads NAME,...] [--noalloc] [--probe-fma]
 
 A step is one C = A . B product of the workload (default: the 4096-cube,
 N(0,1) inputs, seed 2) through the library's C ABI, inputs resident in HBM.
-W untimed steps, then exactly K timed steps bracketed by a barrier and a
-device synchronisation; value = 2*M*N*K*K_steps*ranks / max-over-ranks time.
-Multi-GPU runs are independent replicas (one per rank, no collective on the
-data path): scaling is weak.
+W untimed steps, then exactly K timed steps bracketed by a device
+synchronisation; value = 2*M*N*K*K_steps / time. The library runs on one GPU:
+a multi-rank launch (WORLD_SIZE > 1, or --gpus N > 1) prints an
+"unavailable" line and measures nothing.
 
 Also reported on the same JSON line:
   e2e           the same metric through the same call with host buffers:
@@ -19,25 +20,32 @@ Also reported on the same JSON line:
   roofline      the main kernel's achieved FP32 FLOP/s (CUDA events on its
                 stream) against the FFMA peak SMs x 128 lanes x 2 FLOP x max
                 SM clock ("alu"-bound: the intensity is far above the HBM
-                ridge), with DRAM traffic from the committed ncu summary;
-  cpu_baseline  the FP64 CPU oracle timed on this host's cores: the whole
-                product when it takes under ~30 s, else the sampled rows and
-                columns the parity tests check, else a bounded row sample
-                (--cpu-threads 1 gives the single-core figure);
+                ridge), with DRAM traffic from the committed ncu record
+                (profiles/ffma_tma_sq4096.json);
+  cpu_baseline  the FP64 CPU oracle timed on this host's cores (count and CPU
+                model stated): the whole product when it takes under ~30 s,
+                else the sampled rows and columns the parity tests check,
+                else a bounded row sample (--cpu-threads 1 gives the
+                single-core figure);
   step_ms       median, best and mean device time of the timed steps;
   warm          for workloads that fit in L2 (timed with an L2 flush before
                 every step), the same steps back to back without the flush;
-  clocks        nvidia-smi samples taken during the timed region.
+  clocks        nvidia-smi samples taken during the timed region;
+  workloads     the other named workloads (256^3, 1024^3, 4097x3001x2049,
+                16384^3 by default with the 4096-cube headline), each timed
+                the same way over at least K steps and half a second, with
+                its own clock samples.
 --impl reference times that oracle alone as the reference arm.
 
---probe-fma runs the FP32 FMA throughput probes (FLOP per clock per SM of the
-mainloop's instruction patterns: the ceiling of the main kernel) and exits.
+--probe-fma builds bench_fma_peak.cu and prints the FP32 FMA rate of one SM
+(scalar FFMA and paired FFMA2, loop-invariant operands) against the nominal
+128 lanes x 2 FLOP per clock, then exits.
 
 With --op-a/--op-b/--alpha/--beta/--batch the step is instead one call of
 the general form C_b = alpha * op(A_b) . op(B_b) + beta * C_b over `batch`
 copies of the workload's operands (stored transposed where op = 1), FLOPs
 batch * 2*M*N*K; the step includes any packing pass the call makes. The
-host-buffer, tensor-core and CPU legs are then left out.
+host-buffer, tensor-core, CPU and extra-workload legs are then left out.
 """
 
 from __future__ import annotations
@@ -62,8 +70,11 @@ import workloads  # noqa: E402
 
 FP32_LANES_PER_SM = 128          # FP32 FMA units per SM (4 partitions x 32)
 DEFAULT_SM_MAX_MHZ = 2070.0      # GB300 maximum SM clock
+HEADLINE_WORKLOAD = "sq4096"
+EXTRA_WORKLOADS = ("sq256", "sq1024", "rect4097x3001x2049", "sq16384")
 L2_BYTES = 126.5 * 2 ** 20       # GB300 L2 capacity
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffma_tma_sq4096.md")
+# Machine-readable record of the ncu capture of the headline product kernel.
+PROFILE_RECORD = os.path.join(ROOT, "profiles", "ffma_tma_sq4096.json")
 # The separately reported tensor-core path: 3xTF32 on tcgen05, clusters of
 # two CTAs sharing each B tile by TMA multicast.
 TENSOR_CONFIG = "tf32x3_pair_128x256_k16_s4"
@@ -89,21 +100,9 @@ def intensity(M: int, N: int, K: int) -> float:
     return product_flops(M, N, K) / compulsory_bytes(M, N, K)
 
 
-def max_over_ranks(values, dist_mod=None, device="cpu"):
-    """Element-wise maximum of `values` over all ranks (the slowest rank's
-    times); the values themselves when there is no process group."""
-    if dist_mod is None:
-        return [float(v) for v in values]
-    import torch
-    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
-    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
-    return [float(v) for v in t.tolist()]
-
-
-def job_gflops(flops_per_step: float, steps: int, world: int, seconds: float) -> float:
-    """Whole-job throughput: every rank ran `steps` products in at most
-    `seconds` (weak scaling: each rank has its own problem)."""
-    return flops_per_step * steps * world / seconds / 1e9
+def job_gflops(flops_per_step: float, steps: int, seconds: float) -> float:
+    """Throughput of `steps` products of `flops_per_step` FLOPs in `seconds`."""
+    return flops_per_step * steps / seconds / 1e9
 
 
 def kernel_source_hash() -> str:
@@ -123,21 +122,18 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(config_name: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    summary is missing, is for another kernel config, or predates the
-    current kernel source."""
+    """DRAM bytes per launch of the headline product kernel from the
+    committed ncu record, or None when the record is missing, is for another
+    kernel configuration, or predates the current kernel source."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_RECORD) as f:
+            rec = json.load(f)
+        src, cfg, val = rec["kernel_source_sha256"], rec["kernel_config"], rec["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError, TypeError):
         return None
-    src = re.search(r"kernel_source_sha256:\s*(\w+)", text)
-    cfg = re.search(r"kernel_config:\s*(\S+)", text)
-    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (src and cfg and val):
+    if src != kernel_source_hash() or cfg != config_name or val is None:
         return None
-    if src.group(1) != kernel_source_hash() or cfg.group(1) != config_name:
-        return None
-    return float(val.group(1))
+    return float(val)
 
 
 def measured_tf32_tflops() -> tuple:
@@ -180,7 +176,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", self.gpu_id, "-lms", "50"],
+                 "-i", self.gpu_id, "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -282,7 +278,7 @@ def run_reference(args, world, rank):
         return 0
     import numpy as np
     import oracle
-    w = workloads.WORKLOADS[args.workload]
+    w = shape_workload(args.shape) if args.shape else workloads.WORKLOADS[args.workload]
     oracle.build()
     oracle.set_num_threads(args.cpu_threads if args.cpu_threads > 0 else host_cores())
     A, B = workloads.make_workload(w)
@@ -304,7 +300,7 @@ def run_reference(args, world, rank):
         oracle.sgemm_rows(w.M, w.N, w.K, An, w.lda, Bn, w.ldb,
                           np.sort(rng.choice(w.M, rows_per_step, replace=False)), want_abs=False)
     elapsed = time.perf_counter() - t0
-    value = job_gflops(product_flops(rows_per_step, w.N, w.K), args.steps, 1, elapsed)
+    value = job_gflops(product_flops(rows_per_step, w.N, w.K), args.steps, elapsed)
     sample = f"{rows_per_step} random full rows of C per step ({rows_per_step}x{w.N}x{w.K})"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s",
@@ -313,6 +309,7 @@ def run_reference(args, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, "cpu_oracle_f64", l2="host CPU: no GPU cache involved"),
         "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": oracle.num_threads(),
+                         "cpu_model": cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -379,185 +376,175 @@ def cpu_baseline(w, A, B, threads=0, budget_s=30.0, min_s=10.0):
         unit()
         reps += 1
         dt = time.perf_counter() - t0
-    return {"value": round(job_gflops(done, reps, 1, dt), 3), "unit": "GFLOP/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": round(job_gflops(done, reps, dt), 3), "unit": "GFLOP/s",
+            "cores": oracle.num_threads(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{what} x {reps}, {dt:.1f} s"}
 
 
-FMA_PROBES = ("ffma_loop_invariant", "ffma2_loop_invariant", "ffma_outer_8x8_registers",
-              "ffma2_outer_8x8_registers_fixed", "ffma2_outer_8x8_registers_rotating",
-              "sgemm_inner_loop_8x8_smem", "sgemm_inner_loop_8x16_smem", "sgemm_inner_loop_8x8_smem_12warps",
-              "ffma2_outer_8x8_registers_fixed_swapped", "sgemm_inner_loop_8x16_smem_swapped",
-              "ffma2_outer_8x8_true_pairs_b_reused", "ffma2_outer_8x8_true_pairs_a_reused",
-              "ffma2_outer_8x8_registers_row_serpentine", "ffma2_outer_8x8_registers_column_serpentine",
-              "ffma2_outer_8x16_registers", "ffma2_outer_8x16_registers_row_serpentine",
-              "ffma2_outer_8x16_registers_column_serpentine",
-              "sgemm_inner_loop_8x16_smem_row_serpentine", "sgemm_inner_loop_8x16_smem_column_serpentine",
-              "sgemm_inner_loop_8x8_smem_row_serpentine", "sgemm_inner_loop_8x8_smem_column_serpentine",
-              "sgemm_inner_loop_8x16_smem_zigzag_strips", "sgemm_inner_loop_8x16_smem_column_serpentine_halves",
-              "sgemm_inner_loop_8x16_smem_column_serpentine_reversed_odd_k",
-              "sgemm_inner_loop_8x16_smem_kmajor_a_column_serpentine", "sgemm_inner_loop_8x16_smem_kmajor_a",
-              "sgemm_inner_loop_8x8_smem_kmajor_a_column_serpentine",
-              "sgemm_inner_loop_8x16_smem_kmajor_a_column_serpentine_setmaxnreg_384",
-              "sgemm_inner_loop_8x16_smem_scalar_a_column_serpentine", "sgemm_inner_loop_8x16_smem_scalar_a")
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    platform's processor string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine() or "unknown"
 
 
-def run_fma_probe():
-    """The FP32 FMA throughput probes (dense_fp32_matrix_07_gb300/probe/
-    fma_ceiling.cu): FLOP per clock per SM of each mainloop pattern, against
-    the nominal 128 lanes x 2 FLOP; one JSON line."""
+FMA_PEAK_SRC = os.path.join(ROOT, "bench_fma_peak.cu")
+FMA_PEAK_LIB = os.path.join(ROOT, "_build", "libfma_peak.so")
+
+
+def run_fma_peak():
+    """bench_fma_peak.cu on every SM: FP32 FLOP per clock per SM of scalar
+    FFMA and paired FFMA2 loops against the nominal 128 lanes x 2 FLOP; one
+    JSON line. Built here on demand (the library build never compiles it)."""
     import ctypes
     from dense_fp32_matrix_07_gb300 import build as _b
-    _b.build()
-    lib = ctypes.CDLL(_b.PROBE_LIB)
-    lib.fma_probe_run.restype = ctypes.c_int
+    os.makedirs(os.path.dirname(FMA_PEAK_LIB), exist_ok=True)
+    if not os.path.exists(FMA_PEAK_LIB) or os.path.getmtime(FMA_PEAK_LIB) < os.path.getmtime(FMA_PEAK_SRC):
+        tmp = FMA_PEAK_LIB + f".tmp{os.getpid()}"
+        subprocess.run([_b._nvcc(), *_b.NVCC_FLAGS, "-shared", "-cudart", "static", FMA_PEAK_SRC, "-o", tmp,
+                        "-lpthread", "-ldl", "-lrt"], check=True)
+        os.replace(tmp, FMA_PEAK_LIB)
+    lib = ctypes.CDLL(FMA_PEAK_LIB)
     d = ctypes.c_double
-    lib.fma_probe_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(d), ctypes.POINTER(d),
-                                  ctypes.POINTER(d)]
+    lib.fma_peak_run.restype = ctypes.c_int
+    lib.fma_peak_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(d), ctypes.POINTER(d), ctypes.POINTER(d)]
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     out = {}
-    for kind, name in enumerate(FMA_PROBES):
+    for paired, name in ((0, "ffma"), (1, "ffma2")):
         ms, mhz, flops = d(), d(), d()
-        rc = lib.fma_probe_run(kind, 5, ctypes.byref(ms), ctypes.byref(mhz), ctypes.byref(flops))
+        rc = lib.fma_peak_run(paired, 5, ctypes.byref(ms), ctypes.byref(mhz), ctypes.byref(flops))
         if rc != 0:
-            raise RuntimeError(f"probe {name}: CUDA error {rc}")
+            raise RuntimeError(f"fma peak probe {name}: CUDA error {rc}")
         per_clk = flops.value / (ms.value * 1e-3) / (mhz.value * 1e6) / sms
         out[name] = {"best_ms": round(ms.value, 4), "sm_mhz": round(mhz.value, 1),
+                     "tflops": round(flops.value / (ms.value * 1e-3) / 1e12, 2),
                      "flop_per_clk_per_sm": round(per_clk, 1), "frac_of_256": round(per_clk / 256.0, 4)}
-    print(json.dumps({"probe": "fp32_fma_ceiling", "sms": sms, "nominal_flop_per_clk_per_sm": 256,
+    print(json.dumps({"probe": "fp32_fma_peak", "sms": sms, "nominal_flop_per_clk_per_sm": 256,
                       "results": out}), flush=True)
     return 0
 
 
-def run_l2_probe(mib):
-    """Every SM reads the same `mib` MiB buffer at once (probe/fma_ceiling.cu,
-    l2_probe_shared_read): under ncu, a cold launch's DRAM bytes against the
-    buffer's size show how often the L2 fetches data all SMs share."""
-    import ctypes
-    from dense_fp32_matrix_07_gb300 import build as _b
-    _b.build()
-    lib = ctypes.CDLL(_b.PROBE_LIB)
-    lib.l2_probe_shared_read.restype = ctypes.c_int
-    lib.l2_probe_shared_read.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
-    ms = ctypes.c_double()
-    rc = lib.l2_probe_shared_read(int(mib), 5, ctypes.byref(ms))
-    if rc != 0:
-        raise RuntimeError(f"l2 probe: CUDA error {rc}")
+def parse_shape(text: str):
+    """"MxNxK" -> (M, N, K), each a positive integer."""
+    parts = text.lower().split("x")
+    if len(parts) != 3 or not all(p.isdigit() and int(p) > 0 for p in parts):
+        raise ValueError(f"shape {text!r} is not MxNxK with positive integers")
+    return tuple(int(p) for p in parts)
+
+
+def shape_workload(text: str):
+    """An ad-hoc workload of the given shape: tight strides, N(0,1) inputs
+    from seed 0 (the named workloads' recipe)."""
+    M, N, K = parse_shape(text)
+    return workloads.Workload(f"shape_{M}x{N}x{K}", M, N, K, K, N, N, "normal", 0)
+
+
+def unavailable_multi_gpu(world: int, gpus: int) -> dict:
+    """The line a multi-rank launch of the library's arm prints: the library
+    and its bench run on one GPU; nothing is measured."""
+    n = max(world, gpus)
+    return {"impl": "ours", "metric": METRIC, "n_gpus": n, "value": None, "unit": "GFLOP/s",
+            "unavailable": f"single-GPU library: {n} GPUs requested; the product is one GPU's "
+                           "SGEMM, run one process per GPU for independent products"}
+
+
+def time_steps(step, stream, steps, warmup, flush=None, min_seconds=0.0, max_steps=None, sampler=None):
+    """Runs `warmup` untimed steps, then at least `steps` timed steps (more,
+    up to `max_steps`, until about `min_seconds` of device time), each
+    bracketed by CUDA events on `stream`, with an L2 flush before each when
+    `flush` is given. Returns the per-step device times in ms and the clock
+    summary of `sampler` over the timed region."""
     import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    print(json.dumps({"probe": "l2_shared_read", "mib": mib, "sms": sms, "best_ms": round(ms.value, 4),
-                      "l2_to_sm_gbs": round(sms * mib * 2 ** 20 / (ms.value * 1e-3) / 1e9, 1)}), flush=True)
-    return 0
-
-
-def run_shape_sweep(shapes, config):
-    """Times the product on each "MxNxK" shape (tight strides, N(0,1) inputs
-    drawn on the device from seed 0) back to back, with the automatic
-    configuration or the forced one; one JSON line for the whole sweep. For
-    schedule and selector measurements, not a bench line."""
-    import torch
-    import dense_fp32_matrix_07_gb300 as sg
-    dev = torch.device("cuda", 0)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    peak = sms * FP32_LANES_PER_SM * 2 * measured_sm_max_mhz() * 1e6 / 1e12
-    out = []
-    for shp in shapes:
-        M, N, K = (int(x) for x in shp.lower().split("x"))
-        g = torch.Generator(device=dev).manual_seed(0)
-        A = torch.randn(M, K, device=dev, generator=g)
-        B = torch.randn(K, N, device=dev, generator=g)
-        C = torch.empty(M, N, device=dev)
-        rc, auto_cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(), C.data_ptr(), sms)
-        cfg = config if config >= 0 else auto_cfg
-
-        def call():
-            rc = sg.sgemm_ex(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, cfg, sh)
-            if rc != 0:
-                raise RuntimeError(f"sgemm_ex({shp}, config {cfg}): {sg.sgemm_error_string(rc)}")
-
-        for _ in range(3):
-            call()
-        torch.cuda.synchronize()
-        reps = min(200, max(3, int(3e13 / (2.0 * M * N * K))))
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    n = steps
+    if min_seconds > 0:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(reps):
-            call()
+        step()
         e1.record(stream)
         torch.cuda.synchronize()
-        rc = sg.sgemm_check_status(sh)
-        if rc != 0:
-            raise RuntimeError(f"{shp}: {sg.sgemm_error_string(rc)}")
-        ms = e0.elapsed_time(e1) / reps
-        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-        out.append({"shape": shp, "config": sg.sgemm_config_name(cfg), "reps": reps, "ms": round(ms, 4),
-                    "tflops": round(tf, 2), "fp32_peak_pct": round(100.0 * tf / peak, 2)})
-        del A, B, C
-    print(json.dumps({"sweep": "shapes", "sms": sms, "peak_tflops": round(peak, 3), "results": out}), flush=True)
-    return 0
+        one = max(e0.elapsed_time(e1) / 1e3, 1e-6)
+        n = max(steps, int(min_seconds / one) + 1)
+        if max_steps:
+            n = min(n, max_steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(True)
+    for i in range(n):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    clocks = sampler.stop() if sampler else None
+    return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], clocks
 
 
-def run_config_comparison(shapes, names):
-    """Times each named configuration, forced, on each "MxNxK" shape (tight
-    strides, N(0,1) inputs drawn on the device from seed 0): a 256 MB write
-    between calls, so every call starts with a cold L2, and the median of up
-    to 100 calls or 0.5 s per configuration. One JSON line per shape, for
-    selector studies, not a bench line."""
-    import dense_fp32_matrix_07_gb300 as sg
-    # Names are checked on the host before any device work.
-    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
-    unknown = [n for n in names if n not in ids]
-    if unknown or not names:
-        raise SystemExit(f"unknown configurations: {unknown} (known: {sorted(ids)})")
+def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_id):
+    """One named workload through sgemm() with the automatic configuration:
+    operands drawn by the workloads recipe, at least `steps` timed steps and
+    half a second of device time (L2 flushed between steps when A + B + C
+    fit in it), its own clock samples. Returns the workloads entry."""
     import torch
-    dev = torch.device("cuda", 0)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    stream = torch.cuda.current_stream(dev)
+    A, B = workloads.make_workload(w)
+    dA, dB = A.to(dev), B.to(dev)
+    del A, B
+    dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
     sh = stream.cuda_stream
-    scrub = torch.empty(64 << 20, dtype=torch.float32, device=dev)
-    for shp in shapes:
-        M, N, K = (int(x) for x in shp.lower().split("x"))
-        g = torch.Generator(device=dev).manual_seed(0)
-        A = torch.randn(M, K, device=dev, generator=g)
-        B = torch.randn(K, N, device=dev, generator=g)
-        C = torch.empty(M, N, device=dev)
-        rc, auto_cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, A.data_ptr(), B.data_ptr(), C.data_ptr(), sms)
-        times = {}
-        for name in names:
-            cfg = ids[name]
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    _, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(), dB.data_ptr(),
+                                   dC.data_ptr(), num_sms)
+    total = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev) if total <= L2_BYTES else None
 
-            def call():
-                return sg.sgemm_ex(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, cfg, sh)
+    def step():
+        r = sg.sgemm(w.M, w.N, w.K, dA.data_ptr(), w.lda, dB.data_ptr(), w.ldb, dC.data_ptr(), w.ldc, sh)
+        if r != 0:
+            raise RuntimeError(f"{w.name}: {sg.sgemm_error_string(r)}")
 
-            if call() != 0:
-                times[name] = None
-                continue
-            for _ in range(3):
-                call()
-            torch.cuda.synchronize()
-            ts = []
-            for r in range(100):
-                scrub.fill_(float(r))
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                call()
-                e1.record(stream)
-                e1.synchronize()
-                ts.append(e0.elapsed_time(e1))
-                if sum(ts) > 500.0:
-                    break
-            rc = sg.sgemm_check_status(sh)
-            if rc != 0:
-                raise RuntimeError(f"{shp} {name}: {sg.sgemm_error_string(rc)}")
-            ts.sort()
-            times[name] = round(ts[len(ts) // 2] * 1e3, 1)
-        print(json.dumps({"compare": "configs", "shape": shp, "auto": sg.sgemm_config_name(auto_cfg),
-                          "median_us": times}), flush=True)
-        del A, B, C
-    return 0
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    ms, clocks = time_steps(step, stream, steps, warmup, flush, min_seconds=0.5, max_steps=5000, sampler=sampler)
+    if sg.sgemm_check_status(sh) != 0:
+        raise RuntimeError(f"device status after the {w.name} steps")
+    flops = product_flops(w.M, w.N, w.K)
+    value = job_gflops(flops, len(ms), sum(ms) / 1e3)
+    best = flops / (min(ms) * 1e-3) / 1e9
+    l2 = "flushed between steps" if flush is not None else "A+B+C > L2, no flush"
+    del dA, dB, dC, flush
+    torch.cuda.empty_cache()
+    return {"value": round(value, 1), "unit": "GFLOP/s", "config": sg.sgemm_config_name(cfg),
+            "fp32_peak_pct": round(100.0 * value / 1e3 / peak_tflops, 2),
+            "best_step_fp32_peak_pct": round(100.0 * best / 1e3 / peak_tflops, 2),
+            "steps": len(ms), "launches_per_step": 1 + pa + pb,
+            "step_ms": {"median": round(statistics.median(ms), 4), "best": round(min(ms), 4),
+                        "mean": round(statistics.mean(ms), 4)},
+            "l2": l2,
+            "shape": {"M": w.M, "N": w.N, "K": w.K, "lda": w.lda, "ldb": w.ldb, "ldc": w.ldc,
+                      "dist": w.dist, "seed": w.seed},
+            "clocks": clocks}
 
 
 def main():
@@ -566,13 +553,20 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="sq4096", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--shape", default="", metavar="MxNxK",
+                    help="time an ad-hoc MxNxK product (tight strides, N(0,1) inputs, seed 0) "
+                         "instead of a named workload")
     ap.add_argument("--config", type=int, default=-1, help="force a kernel config id")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs (config sweeps)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs")
     ap.add_argument("--no-tf32x3", action="store_true",
                     help="skip the separately reported 3xTF32 tensor-core measurement")
+    ap.add_argument("--extra-workloads", default=None, metavar="NAME[,NAME...]",
+                    help="other named workloads to time in the same run (default: "
+                         f"{','.join(EXTRA_WORKLOADS)} with the {HEADLINE_WORKLOAD} headline, none "
+                         "otherwise; an empty string: none)")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="oracle threads for cpu_baseline (default: all host cores)")
     ap.add_argument("--op-a", type=int, choices=(0, 1), default=0,
@@ -585,57 +579,54 @@ def main():
     ap.add_argument("--noalloc", action="store_true",
                     help="time the allocation-free entry point sgemm_noalloc instead of sgemm_ex")
     ap.add_argument("--probe-fma", action="store_true",
-                    help="run the FP32 FMA throughput probes (the main kernel's ceiling) and exit")
-    ap.add_argument("--shapes", default="", metavar="MxNxK[,MxNxK...]",
-                    help="time the product on these shapes back to back (automatic or --config) and exit")
-    ap.add_argument("--compare-configs", default="", metavar="NAME[,NAME...]",
-                    help="with --shapes: time each named configuration, forced, on every shape (cold L2, "
-                         "medians) and exit")
-    ap.add_argument("--probe-l2", type=int, default=0, metavar="MIB",
-                    help="every SM reads the same MIB-MiB buffer (L2 sharing probe, for ncu) and exit")
+                    help="run the FP32 FMA peak microbench (bench_fma_peak.cu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.shape:
+        try:
+            parse_shape(args.shape)
+        except ValueError as e:
+            ap.error(str(e))
     world, rank, local = dist_setup()
-
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if world > 1 or args.gpus > 1:
+        # One GPU per product: no rank of a multi-rank launch touches a GPU.
+        if rank == 0:
+            print(json.dumps(unavailable_multi_gpu(world, args.gpus)), flush=True)
+        return 0
     if args.probe_fma:
-        return run_fma_probe()
-    if args.probe_l2:
-        return run_l2_probe(args.probe_l2)
-    if args.shapes and args.compare_configs:
-        return run_config_comparison([x for x in args.shapes.split(",") if x],
-                                     [x for x in args.compare_configs.split(",") if x])
-    if args.shapes:
-        return run_shape_sweep([x for x in args.shapes.split(",") if x], args.config)
+        return run_fma_peak()
+    extra = list(EXTRA_WORKLOADS) if args.extra_workloads is None else \
+        [x for x in args.extra_workloads.split(",") if x]
+    unknown = [x for x in extra if x not in workloads.WORKLOADS]
+    if unknown:
+        ap.error(f"unknown workloads {unknown}")
+    return run_ours(args, local, extra)
 
+
+def run_ours(args, local, extra):
     import torch
     import dense_fp32_matrix_07_gb300 as sg
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-
-    def barrier():
-        if pg is not None:
-            pg.barrier()
-
-    w = workloads.WORKLOADS[args.workload]
+    w = shape_workload(args.shape) if args.shape else workloads.WORKLOADS[args.workload]
     A, B = workloads.make_workload(w)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     general = args.op_a or args.op_b or args.alpha != 1.0 or args.beta != 0.0 or args.batch > 1
     if general or args.noalloc:
-        # The host-buffer, tensor-core and CPU legs belong to the plain sgemm() workload.
+        # The host-buffer, tensor-core, CPU and extra-workload legs belong to
+        # the plain sgemm() workload.
         args.no_e2e = args.no_tf32x3 = args.no_cpu_baseline = True
     if general and args.noalloc:
         raise SystemExit("--noalloc times the plain form only")
+    if general or args.noalloc or args.config >= 0 or args.shape or \
+            (args.extra_workloads is None and w.name != HEADLINE_WORKLOAD):
+        extra = []
     if not general:
         dA, dB = A.to(dev), B.to(dev)
         dC = torch.empty((w.M, w.ldc), dtype=torch.float32, device=dev)
@@ -698,48 +689,22 @@ def main():
     if total_bytes <= L2_BYTES:
         flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if sg.sgemm_check_status(sh) != 0:
-        raise RuntimeError("device status after warm-up")
-
-    sampler = ClockSampler(nvsmi_gpu_id(dev, local))
-    if rank == 0:
-        sampler.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
-    sampler.mark(True)
+    gpu_id = nvsmi_gpu_id(dev, local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    kernel_ms, clocks = time_steps(step, stream, args.steps, args.warmup, flush, sampler=sampler)
     elapsed_host = time.perf_counter() - t0
-    sampler.mark(False)
-    clocks = sampler.stop() if rank == 0 else None
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    step_s = sum(kernel_ms) / 1e3   # device time of the timed steps (flush excluded)
-    if flush is None:
-        step_s = max(step_s, starts[0].elapsed_time(ends[-1]) / 1e3)
     if sg.sgemm_check_status(sh) != 0:
         raise RuntimeError("device status after the timed region")
-
-    (t_max,) = max_over_ranks([step_s], pg, dev)
-    value = job_gflops(flops, args.steps, world, t_max)
+    step_s = sum(kernel_ms) / 1e3   # device time of the timed steps (flush excluded)
+    value = job_gflops(flops, args.steps, step_s)
 
     # An L2-resident workload is also timed warm: the same steps back to
     # back, operands left in L2 by the previous step.
     warm = None
     if flush is not None:
         warm_steps = min(args.steps, 200)
-        barrier()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         for _ in range(warm_steps):
@@ -748,8 +713,8 @@ def main():
         torch.cuda.synchronize()
         if sg.sgemm_check_status(sh) != 0:
             raise RuntimeError("device status after the warm steps")
-        (warm_s,) = max_over_ranks([ev0.elapsed_time(ev1) / 1e3], pg, dev)
-        warm = {"value": round(job_gflops(flops, warm_steps, world, warm_s), 1), "unit": "GFLOP/s",
+        warm_s = ev0.elapsed_time(ev1) / 1e3
+        warm = {"value": round(job_gflops(flops, warm_steps, warm_s), 1), "unit": "GFLOP/s",
                 "steps": warm_steps, "ms_per_step": round(warm_s / warm_steps * 1e3, 4),
                 "note": "back-to-back steps, no L2 flush between them"}
 
@@ -824,15 +789,12 @@ def main():
         e2e_serial(2)
         e2e_pipelined(2)
         torch.cuda.synchronize()
-        barrier()
         serial_s = e2e_serial(e2e_steps)
-        barrier()
         e2e_s = e2e_pipelined(e2e_steps)
         if sg.sgemm_check_status(sh) != 0:
             raise RuntimeError("device status after the e2e steps")
-        e2e_s, serial_s = max_over_ranks([e2e_s, serial_s], pg, dev)
-        e2e_value = job_gflops(flops, e2e_steps, world, e2e_s)
-        serial_value = job_gflops(flops, e2e_steps, world, serial_s)
+        e2e_value = job_gflops(flops, e2e_steps, e2e_s)
+        serial_value = job_gflops(flops, e2e_steps, serial_s)
 
     # ---- the optional 3xTF32 tensor-core path, reported separately ----
     tc = None
@@ -860,7 +822,6 @@ def main():
             tc_step()
         torch.cuda.synchronize()
         tc_steps = max(3, min(args.steps, 50))
-        barrier()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         for _ in range(tc_steps):
@@ -871,8 +832,8 @@ def main():
         torch.cuda.synchronize()
         if sg.sgemm_check_status(sh) != 0:
             raise RuntimeError("device status after the 3xTF32 steps")
-        (tc_s,) = max_over_ranks([ev0.elapsed_time(ev1) / 1e3], pg, dev)
-        tc_value = job_gflops(flops, tc_steps, world, tc_s)
+        tc_s = ev0.elapsed_time(ev1) / 1e3
+        tc_value = job_gflops(flops, tc_steps, tc_s)
         tf32_peak, tf32_basis = measured_tf32_tflops()
         tensor_tflops = 3 * flops * tc_steps / tc_s / 1e12   # three TF32 products per FP32 product
         tc = {"value": round(tc_value, 1), "unit": "GFLOP/s", "config": tc_name, "fallback": tc_fallback,
@@ -883,13 +844,20 @@ def main():
                            "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
                            "frac": round(tensor_tflops / tf32_peak, 4), "peak_basis": tf32_basis}}
 
-    if rank != 0:
-        if pg is not None:
-            pg.destroy_process_group()
-        return 0
-
     sm_max = measured_sm_max_mhz()
     peak_tflops = num_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+
+    # ---- the other named workloads, each timed the same way ----
+    extra_out = None
+    if extra:
+        del s_in, s_mm, s_out
+        if not args.no_e2e:
+            del dA2, dB2, dC2, sets
+        torch.cuda.empty_cache()
+        extra_out = {name: measure_extra_workload(sg, workloads.WORKLOADS[name], dev, stream, args.steps,
+                                                  args.warmup, peak_tflops, gpu_id)
+                     for name in extra}
+
     avg_launch_s = statistics.mean(kernel_ms) / 1e3
     achieved_tflops = flops / avg_launch_s / 1e12
     traffic = None if general else profiled_traffic(cfg_name)
@@ -897,10 +865,10 @@ def main():
         "metric": METRIC,
         "value": round(value, 1),
         "unit": "GFLOP/s",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "ms_per_step": round(step_s / args.steps * 1e3, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -912,7 +880,7 @@ def main():
                                              + (": L2 flushed between steps" if flush is not None else " > L2, no flush"))),
             form={"op_a": args.op_a, "op_b": args.op_b, "alpha": args.alpha, "beta": args.beta,
                   "batch": args.batch}),
-        "fp32_peak_pct": round(100.0 * value / world / 1e3 / peak_tflops, 2),
+        "fp32_peak_pct": round(100.0 * value / 1e3 / peak_tflops, 2),
         "e2e": None if e2e_value is None else {"value": round(e2e_value, 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
                 "d2h_bytes_per_step": int(hC[0].numel() * 4),
@@ -936,15 +904,14 @@ def main():
         "clocks": clocks,
         "host_elapsed_s": round(elapsed_host, 3),
         "tensor_core_3xtf32": tc,
+        "workloads": extra_out,
     }
     if clocks and clocks.get("sm_mhz"):
         line["roofline"]["frac_at_sampled_clock"] = round(
             achieved_tflops / (peak_tflops * clocks["sm_mhz"] / sm_max), 4)
-    if world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, args.cpu_threads)
     print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
     return 0
 
 

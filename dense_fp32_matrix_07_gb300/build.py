@@ -3,8 +3,7 @@
 Each .cu file under csrc/ is compiled to an object in parallel, then linked
 into ``_build/libsgemm.so`` with the CUDA runtime linked statically (so the
 library loads on a machine without a GPU driver; the driver's tensor-map
-encoder is looked up at run time). ``probe/fma_ceiling.cu`` is built beside
-it into ``_build/libfma_probe.so`` (measurement only). Usage: ``python -m
+encoder is looked up at run time). Usage: ``python -m
 dense_fp32_matrix_07_gb300.build [--force] [--verbose-ptxas]``.
 """
 
@@ -22,10 +21,6 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsgemm.so")
-# The FP32 FMA throughput probes behind the main kernel's ceiling (measurement
-# only: bench.py --probe-fma loads it; the product never does).
-PROBE_SRC = os.path.join(HERE, "probe", "fma_ceiling.cu")
-PROBE_LIB = os.path.join(BUILD, "libfma_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
@@ -49,10 +44,10 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB) or not os.path.exists(PROBE_LIB):
+    if not os.path.exists(LIB):
         return False
-    t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
-    return all(os.path.getmtime(p) <= t for p in _deps() + [PROBE_SRC])
+    t = os.path.getmtime(LIB)
+    return all(os.path.getmtime(p) <= t for p in _deps())
 
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
@@ -70,22 +65,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stdout + r.stderr
 
-    def build_probe():
-        tmp = PROBE_LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc, *NVCC_FLAGS, *extra, "-shared", "-cudart", "static", PROBE_SRC, "-o", tmp,
-               "-lpthread", "-ldl", "-lrt"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {PROBE_SRC}:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, PROBE_LIB)
-        return r.stdout + r.stderr
-
-    with cf.ThreadPoolExecutor(max_workers=(jobs or len(sources())) + 1) as ex:
-        probe = ex.submit(build_probe)
+    with cf.ThreadPoolExecutor(max_workers=jobs or len(sources())) as ex:
         results = list(ex.map(compile_one, sources()))
-        probe_log = probe.result()
-    if verbose_ptxas:
-        print(probe_log)
     if verbose_ptxas:
         for _, log in results:
             print(log)

@@ -313,9 +313,11 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     if (!reads_ab) {
         // The empty sum (K == 0) or alpha == 0: C = beta * C.
         if (c.beta == 1.0f) return SGEMM_OK;
-        return launch_scale(c.C, c.M, c.N, c.ldc, c.sc, c.batch, c.beta, stream) == cudaSuccess
-                   ? SGEMM_OK
-                   : SGEMM_ERR_LAUNCH;
+        if (launch_scale(c.C, c.M, c.N, c.ldc, c.sc, c.batch, c.beta, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_LAUNCH;
+        }
+        return SGEMM_OK;
     }
 
     int cfg = -1;

@@ -97,6 +97,14 @@ int noalloc_device(NoAllocDevice **out)
 
 int64_t round_up32(int64_t x) { return (x + 31) / 32 * 32; }
 
+// SGEMM_ERR_LAUNCH after clearing the failed launch's error, so the caller's
+// next cudaGetLastError() does not report it again.
+int launch_failed()
+{
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+}
+
 int64_t extent_elems(int64_t rows, int64_t cols, int64_t ld)
 {
     return (rows == 0 || cols == 0) ? 0 : (rows - 1) * ld + cols;
@@ -168,7 +176,7 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     rc = noalloc_device(&dev);
     if (rc != SGEMM_OK) return rc;
 
-    if (K == 0) return launch_zero_fill(C, M, N, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (K == 0) return launch_zero_fill(C, M, N, ldc, stream) == cudaSuccess ? SGEMM_OK : launch_failed();
 
     int cfg = -1, pack_a = 0, pack_b = 0;
     rc = sgemm_plan(M, N, K, lda, ldb, ldc, a, b, c, dev->num_sms, &cfg, &pack_a, &pack_b);
@@ -205,21 +213,21 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         // The transposed copy, K x M with rows of lda_p floats.
         if (launch_pack_transpose_batched(A, M, K, lda, 0, dev->scratch, lda_p, K * lda_p, 1, stream) !=
             cudaSuccess)
-            return SGEMM_ERR_LAUNCH;
+            return launch_failed();
         g.A = dev->scratch;
         g.lda = lda_p;
         g.op_a = 1;
     } else if (pack_a) {
-        if (pack_into_scratch(A, M, K, lda, 0, lda_p, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        if (pack_into_scratch(A, M, K, lda, 0, lda_p, stream) != cudaSuccess) return launch_failed();
         g.A = dev->scratch;
         g.lda = lda_p;
     }
     if (pack_b) {
         // a_floats is a multiple of 32 floats, so B's copy starts 128-byte aligned.
         if (pack_into_scratch(B, K, N, ldb, a_floats, ldb_p, stream) != cudaSuccess)
-            return SGEMM_ERR_LAUNCH;
+            return launch_failed();
         g.B = dev->scratch + a_floats;
         g.ldb = ldb_p;
     }
-    return launch_config(cfg, g, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    return launch_config(cfg, g, stream) == cudaSuccess ? SGEMM_OK : launch_failed();
 }

@@ -1,5 +1,6 @@
-"""bench.py's JSON line on a GPU: one short run of the 1024^3 workload must
-print every field the bench contract asks for, with consistent values."""
+"""bench.py's JSON line on a GPU: one short run of the 1024^3 workload (with
+the 256^3 workload as its extra-workloads leg) must print every field the
+bench contract asks for, with consistent values."""
 
 import json
 import os
@@ -15,7 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_bench_line_has_every_contract_field(cuda_device):
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "sq1024", "--steps", "5",
-           "--warmup", "3", "--e2e-steps", "2"]
+           "--warmup", "3", "--e2e-steps", "2", "--extra-workloads", "sq256"]
     out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
@@ -51,5 +52,15 @@ def test_bench_line_has_every_contract_field(cuda_device):
     for key in ("value", "unit", "cores", "kind", "sample"):
         assert key in cpu, key
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] > 0
+    assert isinstance(cpu["cpu_model"], str) and cpu["cpu_model"]
+
+    extra = d["workloads"]
+    assert list(extra) == ["sq256"]
+    x = extra["sq256"]
+    assert x["value"] > 0 and x["unit"] == "GFLOP/s" and x["steps"] >= 5
+    assert x["shape"]["M"] == x["shape"]["N"] == x["shape"]["K"] == 256
+    assert x["step_ms"]["best"] <= x["step_ms"]["median"]
+    assert 0 < x["fp32_peak_pct"] < 120 and x["l2"] == "flushed between steps"
+    assert "reasons" in x["clocks"]
 
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]

@@ -1,6 +1,7 @@
 """Host logic of the bench (no GPU): the measurement arithmetic against the
-figures the pages print, the multi-rank aggregation on a world-size-2 gloo
-group, nvidia-smi sample parsing, and the gating of the profiled traffic."""
+figures the pages print, the refusal of multi-rank launches (a world-size-2
+torchrun with gloo ranks on the CPU), nvidia-smi sample parsing, the gating
+of the profiled traffic, and the shape and workload arguments."""
 
 import datetime
 import json
@@ -53,39 +54,53 @@ def test_simple_kernel_tile_footprint_is_the_pages_2176_bytes():
     assert smem == GOLDEN["padded_tile16_smem_bytes"]["value"]
 
 
-def test_job_throughput_is_weak_scaling_over_ranks():
-    # Two ranks each ran 10 steps of 2 GFLOP; the slower took 1 s.
-    assert bench.job_gflops(2e9, 10, 2, 1.0) == pytest.approx(40.0)
-    assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
+def test_job_throughput():
+    # 10 steps of 2 GFLOP in 1 s.
+    assert bench.job_gflops(2e9, 10, 1.0) == pytest.approx(20.0)
 
 
-def _rank_main(rank, world, port, out):
-    os.environ["MASTER_ADDR"] = "127.0.0.1"
-    os.environ["MASTER_PORT"] = str(port)
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    try:
-        # Rank r measured (1 + r) s for the timed steps and (10 - r) s e2e.
-        t = bench.max_over_ranks([1.0 + rank, 10.0 - rank], dist, "cpu")
-        v = bench.job_gflops(4e9, 5, world, t[0])
-        out.put((rank, t, v))
-    finally:
-        dist.destroy_process_group()
+def test_multi_rank_launch_measures_nothing(monkeypatch, capsys):
+    # A world-size-2 launch of the library's arm prints one "unavailable" line
+    # from rank 0 and returns before any device work, so no kernel of the
+    # library (the cluster-pair tensor kernel included) can run on 2 GPUs.
+    def no_device_work(*a, **k):
+        raise AssertionError("a multi-rank launch reached the device path")
+
+    monkeypatch.setattr(bench, "run_ours", no_device_work)
+    monkeypatch.setattr(bench, "run_fma_peak", no_device_work)
+    for rank in ("0", "1"):
+        monkeypatch.setenv("WORLD_SIZE", "2")
+        monkeypatch.setenv("RANK", rank)
+        monkeypatch.setenv("LOCAL_RANK", rank)
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2", "--steps", "3", "--warmup", "3"])
+        assert bench.main() == 0
+        out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+        if rank == "0":
+            assert len(out) == 1
+            d = json.loads(out[0])
+            assert d["value"] is None and d["n_gpus"] == 2 and "single-GPU" in d["unavailable"]
+        else:
+            assert out == []
+    # --gpus 2 without a launcher is refused the same way.
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2", "--probe-fma"])
+    assert bench.main() == 0
+    assert "unavailable" in capsys.readouterr().out
 
 
-def test_max_over_ranks_on_a_two_rank_gloo_group():
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = 29500 + (os.getpid() % 1000)
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    results = sorted(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    for rank, t, v in results:
-        assert t == [2.0, 10.0], (rank, t)          # slowest rank's times everywhere
-        assert v == pytest.approx(4e9 * 5 * 2 / 2.0 / 1e9)
+def test_two_rank_torchrun_launch_prints_one_line():
+    # The launch the multi-GPU contract uses, on CPU gloo ranks: one line,
+    # from rank 0, and neither rank loads the CUDA library.
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(29600 + os.getpid() % 300),
+                        os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["unavailable"]
+    assert "libsgemm" not in r.stderr
 
 
 def _sample(ts, sm, active="Not Active", power_cap="Not Active"):
@@ -111,21 +126,39 @@ def test_short_windows_take_the_nearest_samples():
     assert bench.parse_clock_samples(["garbage\n"], t0, t0 + 1) is None
 
 
-def test_profiled_traffic_is_reported_only_for_the_profiled_kernel():
-    text = open(bench.PROFILE_SUMMARY).read()
-    cfg = re.search(r"kernel_config:\s*(\S+)", text).group(1)
-    src = re.search(r"kernel_source_sha256:\s*(\w+)", text).group(1)
-    if src == bench.kernel_source_hash():
+def test_profiled_traffic_is_reported_only_for_the_profiled_kernel(tmp_path, monkeypatch):
+    rec = json.load(open(bench.PROFILE_RECORD))
+    cfg, src = rec["kernel_config"], rec["kernel_source_sha256"]
+    if src == bench.kernel_source_hash() and rec["dram_bytes_per_launch"] is not None:
         assert bench.profiled_traffic(cfg) > 0
     else:
-        assert bench.profiled_traffic(cfg) is None     # stale summary: no traffic claim
+        assert bench.profiled_traffic(cfg) is None     # stale record: no traffic claim
     assert bench.profiled_traffic("some_other_config") is None
+    # A record of the current source gives its figure; a changed source drops it.
+    fake = tmp_path / "rec.json"
+    fake.write_text(json.dumps({"kernel_config": "k", "kernel_source_sha256": bench.kernel_source_hash(),
+                                "dram_bytes_per_launch": 1.5e8}))
+    monkeypatch.setattr(bench, "PROFILE_RECORD", str(fake))
+    assert bench.profiled_traffic("k") == 1.5e8
+    fake.write_text(json.dumps({"kernel_config": "k", "kernel_source_sha256": "0" * 16,
+                                "dram_bytes_per_launch": 1.5e8}))
+    assert bench.profiled_traffic("k") is None
 
 
-def test_config_comparison_rejects_unknown_names_before_any_device_work():
-    # Runs on a host without a GPU: the names are checked first.
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--shapes", "64x64x64",
-                        "--compare-configs", "ffma2_128x256_k32_s4_ka,no_such_config"],
+def test_shape_argument_gives_a_tight_normal_workload():
+    w = bench.shape_workload("2432x2048x16384")
+    assert (w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.dist, w.seed) == (2432, 2048, 16384, 16384, 2048, 2048,
+                                                                       "normal", 0)
+    for bad in ("12x3", "0x4x4", "axbxc", "4x4x4x4"):
+        with pytest.raises(ValueError):
+            bench.parse_shape(bad)
+
+
+def test_unknown_extra_workload_is_rejected_before_any_device_work():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--extra-workloads", "sq256,nope"],
                        capture_output=True, text=True, cwd=ROOT, timeout=300)
-    assert r.returncode != 0
-    assert "no_such_config" in r.stderr and "ffma2_128x256_k32_s4_ka" in r.stderr
+    assert r.returncode != 0 and "nope" in r.stderr
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
