@@ -33,8 +33,8 @@ Also reported on the same JSON line:
   clocks        nvidia-smi samples taken during the timed region;
   workloads     the other named workloads (256^3, 1024^3, 4097x3001x2049,
                 16384^3 by default with the 4096-cube headline), each timed
-                the same way over at least K steps and half a second, with
-                its own clock samples.
+                the same way over at least min(K, 10) steps and half a
+                second, with its own clock samples.
 --impl reference times that oracle alone as the reference arm.
 
 --probe-fma builds bench_fma_peak.cu and prints the FP32 FMA rate of one SM
@@ -504,9 +504,9 @@ def time_steps(step, stream, steps, warmup, flush=None, min_seconds=0.0, max_ste
 
 def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_id):
     """One named workload through sgemm() with the automatic configuration:
-    operands drawn by the workloads recipe, at least `steps` timed steps and
-    half a second of device time (L2 flushed between steps when A + B + C
-    fit in it), its own clock samples. Returns the workloads entry."""
+    operands drawn by the workloads recipe, at least min(`steps`, 10) timed
+    steps and half a second of device time (L2 flushed between steps when
+    A + B + C fit in it), its own clock samples. Returns the workloads entry."""
     import torch
     A, B = workloads.make_workload(w)
     dA, dB = A.to(dev), B.to(dev)
@@ -526,7 +526,8 @@ def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_i
 
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    ms, clocks = time_steps(step, stream, steps, warmup, flush, min_seconds=0.5, max_steps=5000, sampler=sampler)
+    ms, clocks = time_steps(step, stream, min(steps, 10), warmup, flush, min_seconds=0.5, max_steps=5000,
+                            sampler=sampler)
     if sg.sgemm_check_status(sh) != 0:
         raise RuntimeError(f"device status after the {w.name} steps")
     flops = product_flops(w.M, w.N, w.K)

@@ -31,7 +31,7 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
-            "sgemm_test_withhold_copy", "sgemm_test_launch_without_cluster", "sgemm_test_schedule",
+            "sgemm_test_withhold_copy", "sgemm_test_schedule",
             "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex", "sgemm_general_plan")
 
 _lock = threading.Lock()
@@ -69,9 +69,6 @@ def load(rebuild: bool = False):
                                                 ctypes.c_int, _i64, _vp, _i64, _vp, _vp]
             lib.sgemm_test_fail_next_allocs.restype = ctypes.c_int
             lib.sgemm_test_fail_next_allocs.argtypes = [ctypes.c_int]
-            lib.sgemm_test_launch_without_cluster.restype = ctypes.c_int
-            lib.sgemm_test_launch_without_cluster.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64,
-                                                              _vp, _i64, _vp]
             gen = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
                    _vp, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _i64]
             lib.sgemm_general.restype = ctypes.c_int
@@ -138,25 +135,18 @@ def sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream=0) ->
     return load().sgemm_test_withhold_copy(M, N, K, A, lda, B, ldb, C, ldc, slab, stream)
 
 
-def sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
-    """Test hook: the cluster-pair 3xTF32 configuration with its product
-    kernel launched without its 2-CTA cluster; the kernel detects it, does
-    nothing, and sgemm_check_status() reports SGEMM_ERR_LAUNCH."""
-    return load().sgemm_test_launch_without_cluster(M, N, K, A, lda, B, ldb, C, ldc, stream)
-
-
 def sgemm_test_schedule(M, N, K, bm, bn, bk, slots, policy, batch=1):
     """Test hook (host only): the persistent kernels' work schedule. Returns
-    (items, info): items an (n, 8) int64 array of CTA, tile, first slab, end
-    slab, batch entry, tile row, tile column, partner end (-1 unless the CTA
-    owns a split tile); info a dict of grid, tiles, dp_tiles, sk_ctas, nk,
-    tiles_m, tiles_n."""
+    (items, info): items an (n, 10) int64 array of CTA, tile, first slab, end
+    slab, batch entry, tile row, tile column, and for a part of a split tile
+    its first CTA, last CTA and partial-sum slot (-1 otherwise); info a dict
+    of grid, tiles, dp_tiles, sk_ctas, nk, tiles_m, tiles_n."""
     import numpy as np
     count = ctypes.c_int64(0)
     info = np.zeros(7, dtype=np.int64)
     cap = 1024
     while True:
-        items = np.zeros((cap, 8), dtype=np.int64)
+        items = np.zeros((cap, 10), dtype=np.int64)
         rc = load().sgemm_test_schedule(M, N, K, bm, bn, bk, slots, policy, batch,
                                         items.ctypes.data, cap, ctypes.addressof(count), info.ctypes.data)
         if rc == SGEMM_OK:

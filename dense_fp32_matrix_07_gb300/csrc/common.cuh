@@ -27,10 +27,9 @@ struct GemmArgs {
     unsigned int *status;  // device error word of the current device
     int num_sms;           // streaming multiprocessors of the current device
     int sched = kSchedDataParallel;
-    void *workspace = nullptr;     // stream-K partial sums and flags, or null
+    void *workspace = nullptr;     // stream-K partial sums and arrival counters, or null
     size_t workspace_bytes = 0;
     int withhold_it = -1;          // test hook: CTA 0's producer skips this copy
-    bool test_no_cluster = false;  // test hook: launch cluster kernels without their cluster
     // General form: C_b = alpha * A_b . B_b + beta * C_b for b < batch, with
     // batch strides in elements (a stride of 0 shares one operand).
     float alpha = 1.0f, beta = 0.0f;

@@ -31,17 +31,17 @@
 // same time share A and B panels in L2). Tiles [0, dp_tiles) are whole-tile
 // work, dealt round-robin. The remaining tiles form a stream-K region: their
 // K-slab iterations, taken tile after tile, are cut into sk_ctas contiguous,
-// equal ranges, one per CTA, which evens out the last waves. A range that
-// starts inside a tile leaves a partial sum: the CTA writes it to its own
-// workspace slot and raises one flag per consumer warp. The CTA whose range
-// holds the first slab of that tile owns it: after its own slabs it adds the
-// partial sums of the following CTAs in CTA order (a fixed, deterministic
-// order) and stores the tile. Each consumer warp writes, flags, waits for and
-// reads only its own fragment, so there is no CTA-wide barrier to strand a
-// warp. The cross-CTA waits need all CTAs resident, so such launches are
-// cooperative.
+// equal ranges, one per CTA, which evens out the last waves. A tile whose
+// slabs fall in several ranges is finished by the part that arrives last:
+// every other part writes its partial sum to a slot of its own and bumps the
+// tile's arrival counter (one per consumer warp, each warp handling its own
+// fragment, so no CTA-wide barrier is involved); the part that completes the
+// count adds all parts in CTA order (a fixed, deterministic order) and
+// stores the tile. The CTA holding the tile's first slab usually arrives
+// last; it looks at the counter first and, when every other part is in,
+// adds them straight to its registers. No CTA waits for another.
 //
-// Every wait (mbarrier phase or partial-sum flag) is bounded in time (about a
+// Every mbarrier wait is bounded in time (about a
 // second): on giving up, the thread sets the device error word (read by
 // sgemm_check_status()) and gives up its work; the producer first waits
 // (bounded as well) for every copy it has issued, so no copy can land in the
@@ -333,39 +333,71 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                 }
         }
 
-        if (item.kb0 > 0) {
-            // Partial sum of a tile owned by an earlier CTA: this CTA's slot,
-            // float4 v of consumer thread ct at index v * CONSUMER_THREADS + ct.
-            float4 *slot = reinterpret_cast<float4 *>(sched.partials + (int64_t)g * BM * BN);
+        if (item.kb0 > 0 || item.kb1 < sched.nk) {
+            // A part of a split tile. Each consumer warp handles its own
+            // fragment of the tile: slot layout float4 v of consumer thread
+            // ct at index v * CONSUMER_THREADS + ct, so accesses coalesce.
+            const int first = sk_first_cta(sched, item.tile);
+            const int last = sk_last_cta(sched, item.tile);
+            const unsigned others = (unsigned)(last - first);
+            unsigned *ctr = sched.counters + (item.tile - sched.dp_tiles) * Cfg::CONSUMERS + warp;
+            auto part = [&](int h) {
+                return reinterpret_cast<float4 *>(sched.partials + sk_part_slot(h, first) * (BM * BN));
+            };
+            // The CTA holding the first slab usually finishes its part last:
+            // if every other part has arrived, it adds them to its registers
+            // without writing its own.
+            bool reduce = false;
+            if (g == first) {
+                unsigned seen = 0;
+                if (lane == 0) seen = ld_acquire_gpu(ctr);
+                reduce = __shfl_sync(0xffffffffu, seen, 0) == others;
+            }
+            if (!reduce) {
+                float4 *mine = part(g);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int q = 0; q < G; ++q)
-                    slot[(i * G + q) * Cfg::CONSUMER_THREADS + ct] =
-                        make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(sched.flags + (int64_t)g * Cfg::CONSUMERS + warp, 1u);
-            continue;
-        }
-        if (item.kb1 < sched.nk) {
-            // This CTA owns the tile: add the later CTAs' partial sums in order.
-            const int64_t tile_end = sk_tile_end(sched, item.tile);
-            for (int h = g + 1; sk_holds_part(sched, h, tile_end); ++h) {
-                if (!__all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)h * Cfg::CONSUMERS + warp))) {
-                    if (lane == 0) atomicOr(status, kStatusTimeout);
-                    return;
-                }
-                const float4 *slot = reinterpret_cast<const float4 *>(sched.partials + (int64_t)h * BM * BN);
+                    for (int q = 0; q < G; ++q)
+                        mine[(i * G + q) * Cfg::CONSUMER_THREADS + ct] =
+                            make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
+                __threadfence();
+                __syncwarp();
+                unsigned before = 0;
+                if (lane == 0) before = atomic_inc_acq_rel_gpu(ctr);
+                // Not the last to arrive: that part reduces the tile.
+                if (__shfl_sync(0xffffffffu, before, 0) != others) continue;
+            }
+            // Every part has been published: each lane acquires them itself.
+            (void)ld_acquire_gpu(ctr);
+            // Sum in CTA order first, first + 1, ..., last. The first part is
+            // in this warp's registers when this CTA holds it and has not
+            // written it; otherwise every part is read from its slot.
+            int h0 = first + 1;
+            if (!reduce) {
+                const float4 *p0 = part(first);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
                     for (int q = 0; q < G; ++q) {
-                        const float4 p = slot[(i * G + q) * Cfg::CONSUMER_THREADS + ct];
-                        acc[i][4 * q] += p.x;
-                        acc[i][4 * q + 1] += p.y;
-                        acc[i][4 * q + 2] += p.z;
-                        acc[i][4 * q + 3] += p.w;
+                        const float4 v = p0[(i * G + q) * Cfg::CONSUMER_THREADS + ct];
+                        acc[i][4 * q] = v.x;
+                        acc[i][4 * q + 1] = v.y;
+                        acc[i][4 * q + 2] = v.z;
+                        acc[i][4 * q + 3] = v.w;
+                    }
+            }
+            for (int h = h0; h <= last; ++h) {
+                const float4 *ph = part(h);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int q = 0; q < G; ++q) {
+                        const float4 v = ph[(i * G + q) * Cfg::CONSUMER_THREADS + ct];
+                        acc[i][4 * q] += v.x;
+                        acc[i][4 * q + 1] += v.y;
+                        acc[i][4 * q + 2] += v.z;
+                        acc[i][4 * q + 3] += v.w;
                     }
             }
         }
@@ -513,12 +545,9 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     void *args[] = {&mapA, &mapB, &ep, &s, &status, &withhold};
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false>);
-    // Owners wait on other CTAs' partial sums: all CTAs must be resident.
-    const bool coop = s.sk_ctas > 1;
-    if (coop)
-        e = cudaLaunchCooperativeKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
-    else
-        e = cudaLaunchKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    // No CTA waits for another (split tiles are reduced by their last part),
+    // so this is an ordinary launch.
+    e = cudaLaunchKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

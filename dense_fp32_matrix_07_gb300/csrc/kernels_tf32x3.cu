@@ -24,10 +24,11 @@
 //               TMEM accumulator; tcgen05.commit frees the stage, and at the
 //               end of a tile signals the epilogue;
 //   warps 4-7   epilogue: warp 4+q reads TMEM lanes 32q..32q+31 (rows of the
-//               tile) with tcgen05.ld and stores them to C — or, for a
-//               slab range that does not start a tile, to this CTA's partial
-//               slot (then releases its flag); a tile's owner first adds the
-//               later CTAs' partials, in CTA order.
+//               tile) with tcgen05.ld and stores them to C. For a slab range
+//               of a split tile, the part that arrives last adds every part
+//               in CTA order and stores the tile; the others write their
+//               partial sums to their own slots and count themselves in the
+//               tile's arrival counter (schedule.cuh). No CTA waits for another.
 // The accumulator is double-buffered (2 x 256 of the 512 TMEM columns), so
 // the epilogue of one tile overlaps the MMAs of the next. Every wait is
 // bounded in time; a role that gives up sets the device error word and skips
@@ -106,7 +107,6 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
     // block row rank of the item's CM x 1 group of 128 x BN tiles.
     const int rank = CM > 1 ? (int)ptx::cluster_ctarank() : 0;
     const int g = (int)blockIdx.x / CM;               // schedule index (cluster)
-    const int slot = g * CM + rank;                   // this CTA's partial-sum slot and flags
     const int nk = sched.nk;
     constexpr uint16_t kClusterMask = (uint16_t)((1u << CM) - 1u);
     if constexpr (CM > 1) {
@@ -276,24 +276,77 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
             int tg, tn;
             tile_coords(item.tile, sched.tiles_m, sched.tiles_n, tg, tn);
             const int tm = tg * CM + rank;
-            const bool partial = item.kb0 > 0;                  // slabs of a tile owned earlier
-            const bool owner = item.kb0 == 0 && item.kb1 < nk;  // adds later CTAs' partials
-            int h_end = g + 1;
-            if (owner) {
-                h_end = sk_partner_end(sched, g, item.tile);
-                bool ok = true;
-                for (int h = g + 1; h < h_end && ok; ++h)
-                    ok = __all_sync(0xffffffffu, wait_flag(sched.flags + (int64_t)(h * CM + rank) * 4 + q)) != 0;
-                if (!ok) {
-                    if (lane == 0) atomicOr(status, kStatusTimeout);
-                    break;
-                }
-            }
             // Partial-sum slot layout: float4 v (columns 4v..4v+3) of tile row
             // et at index v * 128 + et, so each warp's accesses are coalesced.
+            // Part h of a split tile (this CTA's rank of cluster h) has the
+            // slot sk_part_slot of CTA index h * CM + rank.
+            const bool split = item.kb0 > 0 || item.kb1 < nk;
+            int first = 0, last = 0;
+            unsigned others = 0;
+            unsigned *ctr = nullptr;
+            bool from_tmem = false;   // reduce now, this part straight from TMEM
+            if (split) {
+                first = sk_first_cta(sched, item.tile);
+                last = sk_last_cta(sched, item.tile);
+                others = (unsigned)(last - first);
+                ctr = sched.counters + ((item.tile - sched.dp_tiles) * CM + rank) * 4 + q;
+                // The part holding the first slab adds the others itself when
+                // they have all arrived; otherwise every part is published.
+                if (g == first) {
+                    unsigned seen = 0;
+                    if (lane == 0) seen = ld_acquire_gpu(ctr);
+                    from_tmem = __shfl_sync(0xffffffffu, seen, 0) == others;
+                    if (from_tmem) (void)ld_acquire_gpu(ctr);
+                }
+            }
+            const bool publish = split && !from_tmem;
+            auto slot_ptr = [&](int h) {
+                const int64_t sl = 2 * ((int64_t)h * CM + rank) + (h == first ? 1 : 0);
+                return reinterpret_cast<float4 *>(sched.partials + sl * (BM * BN));
+            };
             const int64_t row = (int64_t)tm * BM + et;
             float *crow = C + row * ldc;
             const int col_base = tn * BN;
+            // Stores columns c0 .. c0 + 31 of this thread's row of C.
+            auto store_chunk = [&](int c0, float (&f)[32]) {
+                if (row >= M) return;
+                const int col0 = col_base + c0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] *= alpha;
+                if (VEC_C && (int64_t)col0 + 32 <= N) {   // 64-bit: col0 + 32 may reach 2^31
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+                        float4 v = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        if (beta != 0.0f) {
+                            const float4 o = *p;
+                            v.x = fmaf(beta, o.x, v.x);
+                            v.y = fmaf(beta, o.y, v.y);
+                            v.z = fmaf(beta, o.z, v.z);
+                            v.w = fmaf(beta, o.w, v.w);
+                        }
+                        *p = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], f[j]) : f[j];
+                }
+            };
+            // Adds parts h0 .. last of columns c0 .. c0 + 31, in that order.
+            auto add_parts = [&](int h0, int c0, float (&f)[32]) {
+                for (int h = h0; h <= last; ++h) {
+                    const float4 *src = slot_ptr(h);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 p4 = src[((c0 + j) / 4) * 128 + et];
+                        f[j] += p4.x;
+                        f[j + 1] += p4.y;
+                        f[j + 2] += p4.z;
+                        f[j + 3] += p4.w;
+                    }
+                }
+            };
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];
@@ -308,54 +361,40 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap mapAhi, const __grid_con
                 float f[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                if (partial) {
-                    float4 *dst = reinterpret_cast<float4 *>(sched.partials + (int64_t)slot * BM * BN);
+                if (publish) {
+                    float4 *dst = slot_ptr(g);
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         dst[((c0 + j) / 4) * 128 + et] = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
                     continue;
                 }
-                for (int h = g + 1; h < h_end; ++h) {
-                    const float4 *src =
-                        reinterpret_cast<const float4 *>(sched.partials + (int64_t)(h * CM + rank) * BM * BN);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 p4 = src[((c0 + j) / 4) * 128 + et];
-                        f[j] += p4.x;
-                        f[j + 1] += p4.y;
-                        f[j + 2] += p4.z;
-                        f[j + 3] += p4.w;
-                    }
-                }
-                if (row < M) {
-                    const int col0 = col_base + c0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) f[j] *= alpha;
-                    if (VEC_C && (int64_t)col0 + 32 <= N) {   // 64-bit: col0 + 32 may reach 2^31
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
-                            float4 v = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
-                            if (beta != 0.0f) {
-                                const float4 o = *p;
-                                v.x = fmaf(beta, o.x, v.x);
-                                v.y = fmaf(beta, o.y, v.y);
-                                v.z = fmaf(beta, o.z, v.z);
-                                v.w = fmaf(beta, o.w, v.w);
-                            }
-                            *p = v;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], f[j]) : f[j];
-                    }
-                }
+                if (from_tmem) add_parts(first + 1, c0, f);
+                store_chunk(c0, f);
             }
-            if (partial) {
+            if (publish) {
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(sched.flags + (int64_t)slot * 4 + q, 1u);
+                unsigned before = 0;
+                if (lane == 0) before = atomic_inc_acq_rel_gpu(ctr);
+                if (__shfl_sync(0xffffffffu, before, 0) == others) {
+                    // The last part to arrive: every part is in its slot.
+                    (void)ld_acquire_gpu(ctr);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        float f[32];
+                        const float4 *src = slot_ptr(first);
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 p4 = src[((c0 + j) / 4) * 128 + et];
+                            f[j] = p4.x;
+                            f[j + 1] = p4.y;
+                            f[j + 2] = p4.z;
+                            f[j + 3] = p4.w;
+                        }
+                        add_parts(first + 1, c0, f);
+                        store_chunk(c0, f);
+                    }
+                }
             }
         }
         ptx::tc_fence_before();
@@ -575,14 +614,14 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     if ((e = encode_kmajor(&mBh, b_hi, g.N, g.K, l.kp, Cfg::B_PIECE_ROWS, Cfg::BK)) != cudaSuccess) return e;
     if ((e = encode_kmajor(&mBl, b_lo, g.N, g.K, l.kp, Cfg::B_PIECE_ROWS, Cfg::BK)) != cudaSuccess) return e;
 
-    // Stream-K partials and flags (one slot and 4 flags per CTA) follow the
-    // split operands in the workspace.
-    constexpr int kFlags = 4 * Cfg::CM;
+    // Stream-K arrival counters (4 per CTA of a cluster per split tile) and
+    // partial-sum slots (two per CTA) follow the split operands in the workspace.
+    constexpr int kCounters = 4 * Cfg::CM;
     Schedule sched = tf32x3_schedule<Cfg>(g, true);
     if (sched.sk_ctas > 0 &&
-        g.workspace_bytes < l.total + schedule_workspace_bytes(sched, kFlags, Cfg::BM * Cfg::CM, Cfg::BN))
+        g.workspace_bytes < l.total + schedule_workspace_bytes(sched, kCounters, Cfg::BM * Cfg::CM, Cfg::BN))
         sched = tf32x3_schedule<Cfg>(g, false);
-    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, kFlags, stream)) != cudaSuccess)
+    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, kCounters, stream)) != cudaSuccess)
         return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
     float *C = g.C;
@@ -593,20 +632,16 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     void *args[] = {&mAh, &mAl, &mBh, &mBl, &C, &ldc, &M, &N, &sched, &status, &alpha, &beta};
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, true>)
                          : reinterpret_cast<const void *>(sgemm_tf32x3_kernel<Cfg, false>);
-    // Owners wait on other CTAs' partial sums: all CTAs must be resident.
+    // Split tiles are reduced by their last part, so no CTA waits for
+    // another: the only launch attribute is the cluster shape.
     cudaLaunchConfig_t lc = {};
-    cudaLaunchAttribute attrs[2];
+    cudaLaunchAttribute attrs[1];
     int na = 0;
-    if (Cfg::CM > 1 && !g.test_no_cluster) {
+    if (Cfg::CM > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = Cfg::CM;
         attrs[na].val.clusterDim.y = 1;
         attrs[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    if (sched.sk_ctas > 1) {
-        attrs[na].id = cudaLaunchAttributeCooperative;
-        attrs[na].val.cooperative = 1;
         ++na;
     }
     lc.gridDim = dim3((unsigned)(sched.grid * Cfg::CM));

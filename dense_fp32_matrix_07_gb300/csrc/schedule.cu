@@ -5,9 +5,9 @@ namespace sgemm_gb300 {
 
 namespace {
 size_t round_up_bytes(size_t x, size_t a) { return (x + a - 1) / a * a; }
-size_t flag_bytes(const Schedule &s, int flags_per_cta)
+size_t counter_bytes(const Schedule &s, int counters_per_tile)
 {
-    return round_up_bytes((size_t)s.sk_ctas * flags_per_cta * sizeof(unsigned), 256);
+    return round_up_bytes((size_t)(s.tiles - s.dp_tiles) * counters_per_tile * sizeof(unsigned), 256);
 }
 }  // namespace
 
@@ -68,18 +68,18 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
     return s;
 }
 
-size_t schedule_workspace_bytes(const Schedule &s, int flags_per_cta, int bm, int bn)
+size_t schedule_workspace_bytes(const Schedule &s, int counters_per_tile, int bm, int bn)
 {
     if (s.sk_ctas == 0) return 0;
-    return flag_bytes(s, flags_per_cta) + (size_t)s.sk_ctas * bm * bn * sizeof(float);
+    return counter_bytes(s, counters_per_tile) + 2 * (size_t)s.sk_ctas * bm * bn * sizeof(float);
 }
 
-cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int flags_per_cta, cudaStream_t stream)
+cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, cudaStream_t stream)
 {
-    const size_t fb = flag_bytes(s, flags_per_cta);
-    s.flags = static_cast<unsigned *>(workspace);
-    s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + fb);
-    return cudaMemsetAsync(s.flags, 0, fb, stream);
+    const size_t cb = counter_bytes(s, counters_per_tile);
+    s.counters = static_cast<unsigned *>(workspace);
+    s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cb);
+    return cudaMemsetAsync(s.counters, 0, cb, stream);
 }
 
 }  // namespace sgemm_gb300

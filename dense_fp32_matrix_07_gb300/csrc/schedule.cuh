@@ -1,12 +1,13 @@
 // Work schedule shared by the persistent kernels: output tiles in groups of 8
 // block rows; whole tiles dealt round-robin for all but the last one or two
 // waves; the remaining tiles' K-slab iterations cut into equal contiguous
-// ranges, one per CTA (stream-K). A range that starts inside a tile leaves a
-// partial sum in the CTA's workspace slot, published with release flags; the
-// CTA whose range holds the tile's first slab (its owner) adds the later
-// CTAs' partials in CTA order, a fixed order, so results are deterministic.
-// Waits only ever point to higher CTA indices, so they cannot form a cycle;
-// launches with such waits must be cooperative (all CTAs resident).
+// ranges, one per CTA (stream-K). A tile whose slabs fall in several CTAs'
+// ranges is reduced by whichever of them finishes its part last: each part
+// that is not last writes its partial sum to a slot of its own and counts
+// itself in the tile's arrival counter; the part that completes the count
+// adds every part in CTA order (a fixed order, so results are
+// deterministic) and stores the tile. No CTA ever waits for another, so no
+// launch needs all its CTAs resident at once.
 #pragma once
 
 #include "common.cuh"
@@ -21,22 +22,12 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
     return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
+// Adds 1 with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atomic_inc_acq_rel_gpu(unsigned *p)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Waits until *flag != 0; false after kWaitLimitNs.
-__device__ __forceinline__ bool wait_flag(const unsigned *flag)
-{
-    if (ld_acquire_gpu(flag) != 0) return true;
-    const uint64_t t0 = ptx::global_timer_ns();
-    for (uint32_t n = 0; n < kSpinLimit; ++n) {
-        __nanosleep(64);
-        if (ld_acquire_gpu(flag) != 0) return true;
-        if (ptx::global_timer_ns() - t0 > ptx::kWaitLimitNs) return false;
-    }
-    return false;
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
 }
 
 // The work schedule, computed on the host (plan_schedule) and read by every
@@ -50,8 +41,8 @@ struct Schedule {
     int64_t dp_tiles;   // whole-tile work: tiles [0, dp_tiles), round-robin
     int64_t sk_iters;   // slab iterations of the stream-K region
     int sk_ctas;        // CTAs [0, sk_ctas) share those iterations
-    unsigned *flags;    // sk_ctas x (flags per CTA), zeroed before the launch
-    float *partials;    // sk_ctas slots of BM x BN floats
+    unsigned *counters; // arrival counters: (tiles - dp_tiles) x (counters per tile), zeroed before the launch
+    float *partials;    // 2 x sk_ctas slots of BM x BN floats (sk_slot)
 };
 
 // One unit of work: slabs [kb0, kb1) of output tile `tile`.
@@ -70,29 +61,39 @@ __host__ __device__ __forceinline__ int64_t sk_start(const Schedule &s, int g)
     return s.sk_iters * g / s.sk_ctas;
 }
 
-// Stream-K iteration one past the last slab of stream-K tile `tile`.
-__host__ __device__ __forceinline__ int64_t sk_tile_end(const Schedule &s, int64_t tile)
+// The CTAs whose ranges hold slabs of stream-K tile `tile` are
+// sk_first_cta .. sk_last_cta. CTA g's range starts at floor(S g / C)
+// (S = sk_iters, C = sk_ctas), so the CTA holding iteration x is the largest
+// g with floor(S g / C) <= x, i.e. ceil((x + 1) C / S) - 1. Every range is
+// non-empty (plan_schedule keeps sk_ctas <= sk_iters).
+__host__ __device__ __forceinline__ int sk_cta_of_iter(const Schedule &s, int64_t x)
 {
-    return (tile - s.dp_tiles + 1) * s.nk;
+    return (int)(((x + 1) * s.sk_ctas + s.sk_iters - 1) / s.sk_iters - 1);
 }
 
-// Whether CTA h, above the owner of a stream-K tile ending at iteration
-// `tile_end`, still holds slabs of that tile (its range starts before the
-// end). The owner's partners are g+1, g+2, ... while this holds.
-__host__ __device__ __forceinline__ bool sk_holds_part(const Schedule &s, int h, int64_t tile_end)
+__host__ __device__ __forceinline__ int sk_first_cta(const Schedule &s, int64_t tile)
 {
-    return h < s.sk_ctas && sk_start(s, h) < tile_end;
+    return sk_cta_of_iter(s, (tile - s.dp_tiles) * s.nk);
 }
 
-// For the owner g of stream-K tile `tile` (the CTA holding its first slab):
-// one past the last CTA whose range holds later slabs of that tile. The
-// owner adds the partial sums of CTAs g+1 .. end-1, in that order.
-__host__ __device__ __forceinline__ int sk_partner_end(const Schedule &s, int g, int64_t tile)
+__host__ __device__ __forceinline__ int sk_last_cta(const Schedule &s, int64_t tile)
 {
-    const int64_t tile_end = sk_tile_end(s, tile);
-    int h = g + 1;
-    while (sk_holds_part(s, h, tile_end)) ++h;
-    return h;
+    return sk_cta_of_iter(s, (tile - s.dp_tiles + 1) * s.nk - 1);
+}
+
+// Partial-sum slot of CTA g's part of a split tile. A CTA holds at most two
+// such parts: the first item of its range, which may start inside a tile
+// (kb0 > 0), and the last, which may end inside one (it then starts at the
+// tile's first slab). They take slots 2g and 2g + 1, so no slot is written
+// twice in one launch. The part of sk_first_cta is the one starting at slab 0.
+__host__ __device__ __forceinline__ int64_t sk_slot(int g, int kb0)
+{
+    return 2 * (int64_t)g + (kb0 == 0 ? 1 : 0);
+}
+
+__host__ __device__ __forceinline__ int64_t sk_part_slot(int h, int first)
+{
+    return sk_slot(h, h == first ? 0 : 1);
 }
 
 __host__ __device__ __forceinline__ Cursor cursor_init(const Schedule &s, int g)
@@ -166,12 +167,13 @@ __host__ __device__ __forceinline__ void tile_coords_b(const Schedule &s, int64_
 Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
                        bool with_sk, int64_t batch = 1);
 
-// Workspace bytes of a stream-K schedule: flags (`flags_per_cta` per CTA,
-// rounded to 256 bytes) then one bm x bn FP32 partial-sum slot per CTA.
-size_t schedule_workspace_bytes(const Schedule &s, int flags_per_cta, int bm, int bn);
+// Workspace bytes of a stream-K schedule: the arrival counters
+// (`counters_per_tile` per stream-K tile, rounded up to 256 bytes), then two
+// bm x bn FP32 partial-sum slots per CTA of the stream-K region.
+size_t schedule_workspace_bytes(const Schedule &s, int counters_per_tile, int bm, int bn);
 
-// Points the schedule's flags and partial slots into `workspace` and zeroes
-// the flags on `stream`.
-cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int flags_per_cta, cudaStream_t stream);
+// Points the schedule's counters and partial slots into `workspace` and
+// zeroes the counters on `stream`.
+cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, cudaStream_t stream);
 
 }  // namespace sgemm_gb300

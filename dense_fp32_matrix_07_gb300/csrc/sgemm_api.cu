@@ -208,7 +208,6 @@ struct Call {
     int config;          // -1: automatic
     int sched_override;  // -1: the configuration's policy (test knob)
     int withhold_it;     // -1: none (test knob)
-    bool no_cluster = false;  // test knob: cluster kernels launched without their cluster
 };
 
 // Elements spanned by `batch` entries of extent `e` at stride `s`, or -1.
@@ -328,7 +327,6 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
     g.sched = c.sched_override >= 0 ? c.sched_override : kConfigTable[cfg].sched;
     g.withhold_it = c.withhold_it;
-    g.test_no_cluster = c.no_cluster;
     g.alpha = c.alpha;
     g.beta = c.beta;
     g.batch = c.batch;
@@ -449,14 +447,6 @@ int sgemm_test_fail_next_allocs(int n)
     return SGEMM_OK;
 }
 
-int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
-                                      const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream)
-{
-    Call c{0, 0, M, N, K, 1.0f, A, lda, 0, B, ldb, 0, 0.0f, C, ldc, 0, 1, kCfgTf32x3_pair, -1, -1};
-    c.no_cluster = true;
-    return sgemm_call(c, stream);
-}
-
 int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, int64_t slots, int policy,
                         int64_t batch, int64_t *items, int64_t capacity, int64_t *count, int64_t *info)
 {
@@ -479,8 +469,8 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
             if (n < capacity) {
                 int b, tm, tn;
                 tile_coords_b(s, it.tile, b, tm, tn);
-                const bool owner = it.kb0 == 0 && it.kb1 < s.nk;
-                int64_t *r = items + 8 * n;
+                const bool split = it.kb0 > 0 || it.kb1 < s.nk;
+                int64_t *r = items + 10 * n;
                 r[0] = g;
                 r[1] = it.tile;
                 r[2] = it.kb0;
@@ -488,7 +478,9 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
                 r[4] = b;
                 r[5] = tm;
                 r[6] = tn;
-                r[7] = owner ? sk_partner_end(s, g, it.tile) : -1;
+                r[7] = split ? sk_first_cta(s, it.tile) : -1;
+                r[8] = split ? sk_last_cta(s, it.tile) : -1;
+                r[9] = split ? sk_slot(g, it.kb0) : -1;
             }
             ++n;
         }

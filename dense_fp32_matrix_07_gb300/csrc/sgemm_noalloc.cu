@@ -13,9 +13,10 @@
 // them; later calls on the device reuse the cache. Make that first call
 // before any stream capture begins.
 //
-// A second fixed array, 24 MiB, holds the stream-K partial sums and flags of
-// the product's schedule (at most one 128 x 256 tile per SM: about 19 MiB on
-// 152 SMs); a schedule that would need more runs whole tiles instead.
+// A second fixed array, 48 MiB, holds the stream-K partial sums and arrival
+// counters of the product's schedule (at most two 128 x 256 tiles per SM:
+// about 38 MiB on 152 SMs); a schedule that would need more runs whole tiles
+// instead.
 //
 // Where sgemm() would take a k-major configuration (one that reads A as a
 // transposed copy), this entry point makes that copy in its fixed array when
@@ -25,8 +26,8 @@
 // Sharing: every call on a device uses the same arrays, which keep whatever
 // the last call left in them. Nothing in it has to start at zero (each call
 // rewrites every packed entry the product reads, the padding at the end of
-// packed rows is never read, and the stream-K flags are zeroed by a memset on
-// the call's stream before its product). Calls whose work overlaps on the
+// packed rows is never read, and the stream-K arrival counters are zeroed by
+// a memset on the call's stream before its product). Calls whose work overlaps on the
 // GPU (different streams, or different host threads) race on the array and
 // must be ordered by the caller.
 #include "../../include/sgemm.h"
@@ -43,9 +44,10 @@ constexpr int64_t kNoAllocScratchFloats = int64_t(16) << 20;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-// 24 MiB for the stream-K partial sums and flags: one 128 x 256 FP32 tile
-// (128 KiB) per CTA slot for up to 190 SMs, with room for the flags.
-constexpr size_t kNoAllocWorkspaceBytes = size_t(24) << 20;
+// 48 MiB for the stream-K partial sums and arrival counters: two 128 x 256
+// FP32 tiles (2 x 128 KiB) per CTA slot for up to 190 SMs, with room for the
+// counters.
+constexpr size_t kNoAllocWorkspaceBytes = size_t(48) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
 
@@ -198,7 +200,7 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         return SGEMM_ERR_SCRATCH_LIMIT;
 
     GemmArgs g{M, N, K, A, lda, B, ldb, C, ldc, dev->status, dev->num_sms};
-    // The stream-K partial sums and flags go in the fixed workspace array
+    // The stream-K partial sums and counters go in the fixed workspace array
     // when they fit (they always do on GPUs of up to 190 SMs); otherwise the
     // product runs whole tiles, which need no workspace.
     g.sched = kSchedAuto;

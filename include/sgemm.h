@@ -29,14 +29,15 @@
  * frees, retains or reads host memory through it. Scratch space the library
  * needs (a packed copy of an operand whose rows are not 16-byte aligned, the
  * transposed K x M copy of A that the k-major configurations read, the
- * partial sums and flags of a stream-K tail, the hi/lo operand planes of the
- * 3xTF32 configurations) is taken from a library-owned, stream-ordered
+ * partial sums and arrival counters of a stream-K tail, the hi/lo operand
+ * planes of the 3xTF32 configurations) is taken from a library-owned,
+ * stream-ordered
  * memory pool on `stream` and returned on `stream`; it is never exposed.
  * Asynchrony: calls return after enqueueing work on `stream`; results are
  * ready when the stream's work completes. An FFMA call enqueues at most
  * three kernels (operand packing, then the product) plus a memset of the
- * stream-K flags; a 3xTF32 call enqueues two split passes and the product
- * per batch entry. No call synchronises the host.
+ * stream-K arrival counters; a 3xTF32 call enqueues two split passes and
+ * the product per batch entry. No call synchronises the host.
  * Graph capture: sgemm(), sgemm_ex(), sgemm_general() and sgemm_general_ex()
  * may be captured into a CUDA graph once one call has run on the device
  * (the first call sets the device up); a replay computes the product of
@@ -272,24 +273,6 @@ int sgemm_test_withhold_copy(int64_t M, int64_t N, int64_t K,
                              int slab, cudaStream_t stream);
 
 /*
- * sgemm_test_launch_without_cluster — test hook for the launch-shape check
- * of the cluster-pair 3xTF32 kernel (configuration
- * "tf32x3_pair_128x256_k16_s4"; the pages have no counterpart).
- *
- * Runs that configuration, but launches its product kernel without the
- * 2-CTA cluster it needs. The kernel's first action is to compare its
- * cluster size with 2; finding 1, it sets the device error word and returns
- * without touching shared memory, barriers or C. The call returns SGEMM_OK
- * (the launch itself succeeds), sgemm_check_status() then returns
- * SGEMM_ERR_LAUNCH, and C is unchanged. Arguments as sgemm() (the split
- * pre-passes still run into library-owned scratch).
- */
-int sgemm_test_launch_without_cluster(int64_t M, int64_t N, int64_t K,
-                                      const float *A, int64_t lda,
-                                      const float *B, int64_t ldb,
-                                      float *C, int64_t ldc, cudaStream_t stream);
-
-/*
  * sgemm_test_fail_next_allocs — test hook for the allocation-failure paths
  * (the pages have no counterpart).
  *
@@ -311,11 +294,13 @@ int sgemm_test_fail_next_allocs(int n);
  * tiles of bk-deep slabs on `slots` CTAs under `policy` (0 automatic, 1 whole
  * tiles, 2 stream-K everywhere, 3 tail split), with the stream-K workspace
  * available, and walks every CTA's work items in the order the kernels do.
- * Item n fills items[8n .. 8n+7]: CTA, tile, first slab, end slab, batch
- * entry, tile row, tile column, and, for the owner of a tile split among
- * several CTAs (it holds the first slab), one past the last CTA whose
- * partial sums it adds (else -1). info[0..6] receive the grid, tiles, whole
- * tiles, stream-K CTAs, slabs per tile, tile rows and tile columns.
+ * Item n holds: CTA, tile, first slab, end slab, batch
+ * entry, tile row, tile column, and, for a part of a tile split among
+ * several CTAs, the first and the last of those CTAs and the partial-sum
+ * slot this part writes when it does not reduce the tile (else -1, -1, -1).
+ * Items take 10 entries each: items[10n .. 10n+9]. info[0..6] receive the
+ * grid, tiles, whole tiles, stream-K CTAs, slabs per tile, tile rows and
+ * tile columns.
  * *count receives the number of items; SGEMM_ERR_INVALID_VALUE if it exceeds
  * `capacity` (items then holds the first `capacity`) or an argument is out
  * of range.
@@ -337,8 +322,9 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
  * 16-byte aligned, or a leading dimension that is not a multiple of 4
  * floats) and for the partial sums of a stream-K tail; this entry point packs
  * such operands into a fixed scratch array compiled into the library instead,
- * keeps the stream-K partial sums and flags in a second fixed array (24 MiB;
- * a schedule needing more, on GPUs of over 190 SMs, runs whole tiles), and
+ * keeps the stream-K partial sums and arrival counters in a second fixed
+ * array (48 MiB; a schedule needing more, on GPUs of over 190 SMs, runs
+ * whole tiles), and
  * allocates nothing. Where sgemm() would take a k-major configuration, this
  * entry point makes its transposed copy of A in the fixed array when that
  * fits (K * round_up(M, 32) floats, beside a packed B), and otherwise runs
@@ -352,7 +338,7 @@ int sgemm_test_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk,
  * enqueued. Aligned operands are not packed and have no size limit.
  *
  * Memory: every GPU that loads the library's device code holds the two
- * arrays (64 MiB + 24 MiB) until the process exits.
+ * arrays (64 MiB + 48 MiB) until the process exits.
  * Set-up: the first call on a device (with that device current) looks up the
  * arrays' device addresses and caches them with the device's other
  * constants; make that first call before any stream capture begins.

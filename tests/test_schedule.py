@@ -2,13 +2,14 @@
 
 sgemm_test_schedule() walks every CTA's work items with the same functions
 the kernels run (plan_schedule, cursor_init, next_item, tile_coords_b,
-sk_partner_end). For every shape and policy here:
+sk_first_cta, sk_last_cta, sk_slot). For every shape and policy here:
   - every (tile, slab) of the product is computed exactly once;
   - whole tiles precede the stream-K region, whose items are slab ranges;
-  - a tile split among several CTAs has exactly one owner (the CTA holding
-    its first slab), and the partner range the owner adds equals the set of
-    CTAs holding the tile's other slabs, all of higher index than the owner
-    (waits point upwards only, so they cannot form a cycle);
+  - the parts of a tile split among several CTAs come from exactly the
+    consecutive CTAs first .. last that the kernels add in that order, and
+    the first of them holds the tile's first slab;
+  - no two parts write the same partial-sum slot in one launch, and every
+    slot lies inside the 2 x sk_ctas slots of the workspace;
   - tile coordinates are distinct and inside the tile grid of each entry;
   - each CTA's items follow one another in order of iteration.
 """
@@ -47,7 +48,7 @@ def _check(M, N, K, bm, bn, bk, slots, batch, policy):
     assert tiles == tiles_m * tiles_n * batch
     grid, dp_tiles, sk_ctas = info["grid"], info["dp_tiles"], info["sk_ctas"]
     assert 1 <= grid <= max(slots, 1) and 0 <= sk_ctas <= grid and 0 <= dp_tiles <= tiles
-    cta, tile, kb0, kb1, b, tm, tn, pend = (items[:, i] for i in range(8))
+    cta, tile, kb0, kb1, b, tm, tn, first, last, slot = (items[:, i] for i in range(10))
     assert np.all((0 <= cta) & (cta < grid))
     assert np.all((0 <= kb0) & (kb0 < kb1) & (kb1 <= nk))
 
@@ -66,20 +67,25 @@ def _check(M, N, K, bm, bn, bk, slots, batch, policy):
         assert coords[int(t)] == (bb, r, c)
     assert len(set(coords.values())) == tiles
 
-    # Owners and partners of split tiles.
+    # Parts of split tiles.
     pieces = {}
-    for g, t, a, e, p in zip(cta, tile, kb0, kb1, pend):
-        pieces.setdefault(int(t), []).append((int(a), int(e), int(g), int(p)))
+    for g, t, a, e, f, l, sl in zip(cta, tile, kb0, kb1, first, last, slot):
+        pieces.setdefault(int(t), []).append((int(a), int(e), int(g), int(f), int(l), int(sl)))
+    used_slots = set()
     for t, ps in pieces.items():
         if len(ps) == 1:
-            assert ps[0][3] == -1                          # one CTA computes the whole tile
+            assert ps[0][3:] == (-1, -1, -1)               # one CTA computes the whole tile
             continue
-        owners = [p for p in ps if p[0] == 0]
-        assert len(owners) == 1, (t, ps)
-        _, _, g_own, p_end = owners[0]
-        others = sorted(p[2] for p in ps if p[0] > 0)
-        assert others == list(range(g_own + 1, p_end)), (t, g_own, p_end, others)
-        assert all(p[3] == -1 for p in ps if p[0] > 0)
+        ctas = sorted(p[2] for p in ps)
+        f, l = ps[0][3], ps[0][4]
+        assert all((p[3], p[4]) == (f, l) for p in ps), (t, ps)
+        assert ctas == list(range(f, l + 1)), (t, ctas, f, l)
+        assert [p[2] for p in ps if p[0] == 0] == [f]       # the first part starts the tile
+        for a, _, g, _, _, sl in ps:
+            assert sl == 2 * g + (1 if a == 0 else 0)
+            assert 0 <= sl < 2 * sk_ctas
+            assert sl not in used_slots, (t, sl)
+            used_slots.add(sl)
 
     # Each CTA's items in increasing order of (tile, slab) iteration.
     for g in range(grid):
