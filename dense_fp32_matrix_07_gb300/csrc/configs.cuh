@@ -98,6 +98,10 @@ cudaError_t configs_prepare_device();
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream);
 size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g);
 cudaError_t prepare_ffma_tma();
+// The same kernels trimming the last K slab, for K not a multiple of the
+// slab depth (kernels_ffma_tma_ktail.cu); launch_ffma_tma() dispatches there.
+cudaError_t launch_ffma_tma_ktail(int kernel, const GemmArgs &g, cudaStream_t stream);
+cudaError_t prepare_ffma_tma_ktail();
 
 // Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
 cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);

@@ -18,6 +18,7 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
     s.tiles_m = (int)((M + bm - 1) / bm);
     s.tiles_n = (int)((N + bn - 1) / bn);
     s.nk = (int)((K + bk - 1) / bk);
+    s.k_last = (int)(K - (int64_t)(s.nk - 1) * bk);
     s.tiles_per_batch = (int64_t)s.tiles_m * s.tiles_n;
     s.tiles = s.tiles_per_batch * (batch > 0 ? batch : 1);
     s.dp_tiles = s.tiles;

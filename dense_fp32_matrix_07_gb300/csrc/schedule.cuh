@@ -36,6 +36,7 @@ struct Schedule {
     int tiles_m, tiles_n;
     int64_t tiles_per_batch;   // tiles_m * tiles_n
     int nk;             // K slabs per tile
+    int k_last;         // k of the last slab that hold data (1 .. bk)
     int grid;           // CTAs launched
     int64_t tiles;      // all output tiles, batch entry after batch entry
     int64_t dp_tiles;   // whole-tile work: tiles [0, dp_tiles), round-robin
