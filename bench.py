@@ -540,7 +540,8 @@ def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_i
     return {"value": round(value, 1), "unit": "GFLOP/s", "config": sg.sgemm_config_name(cfg),
             "fp32_peak_pct": round(100.0 * value / 1e3 / peak_tflops, 2),
             "best_step_fp32_peak_pct": round(100.0 * best / 1e3 / peak_tflops, 2),
-            "steps": len(ms), "launches_per_step": 1 + pa + pb,
+            "steps": len(ms),
+            "launches_per_step": 1 + pa + pb + (1 if sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1] > 0 else 0),
             "step_ms": {"median": round(statistics.median(ms), 4), "best": round(min(ms), 4),
                         "mean": round(statistics.mean(ms), 4)},
             "l2": l2,
@@ -642,7 +643,10 @@ def run_ours(args, local, extra):
             if w.K * r32(w.M) + (w.K * r32(w.N) if pb else 0) > (16 << 20):
                 cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
                 pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
-        launches_per_step = 1 + pa + pb
+        # The packs, the product and, for an M just past a multiple of the
+        # block height, the kernel of the last rows (sgemm_noalloc has none).
+        tail = 0 if args.noalloc else sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1]
+        launches_per_step = 1 + pa + pb + (1 if tail > 0 else 0)
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
         flops = product_flops(w.M, w.N, w.K)
 
@@ -673,7 +677,8 @@ def run_ours(args, local, extra):
         if rc != 0:
             raise SystemExit(f"general form: {sg.sgemm_error_string(rc)}")
         packs = sg.sgemm_config_name(cfg).startswith("ffma")
-        launches_per_step = (1 + pa + pb) if packs else 3 * args.batch
+        tail = sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K, args.batch)[1]
+        launches_per_step = (1 + pa + pb + (1 if tail > 0 else 0)) if packs else 3 * args.batch
         total_bytes = 4 * args.batch * (sa + sb + sc)
         flops = args.batch * product_flops(w.M, w.N, w.K)
 
@@ -900,7 +905,8 @@ def run_ours(args, local, extra):
                      "peak_basis": f"{num_sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
                                    f"{sm_max:.0f} MHz (max SM clock)",
                      "achieved_basis": ("2MNK / mean CUDA-event time of one call: the product kernel"
-                                        + (f" and its {launches_per_step - 1} operand pack(s)"
+                                        + (f" with {launches_per_step - 1} other launch(es): operand "
+                                           "packs and the last-rows kernel"
                                            if launches_per_step > 1 else "")
                                         + ", on the launching stream")},
         "clocks": clocks,

@@ -31,7 +31,7 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 # Every function declared in include/sgemm.h.
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
-            "sgemm_test_withhold_copy", "sgemm_test_schedule",
+            "sgemm_test_withhold_copy", "sgemm_test_schedule", "sgemm_plan_row_tail",
             "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex", "sgemm_general_plan")
 
 _lock = threading.Lock()
@@ -67,6 +67,8 @@ def load(rebuild: bool = False):
             lib.sgemm_test_schedule.restype = ctypes.c_int
             lib.sgemm_test_schedule.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64,
                                                 ctypes.c_int, _i64, _vp, _i64, _vp, _vp]
+            lib.sgemm_plan_row_tail.restype = ctypes.c_int
+            lib.sgemm_plan_row_tail.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64, _vp]
             lib.sgemm_test_fail_next_allocs.restype = ctypes.c_int
             lib.sgemm_test_fail_next_allocs.argtypes = [ctypes.c_int]
             gen = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
@@ -194,6 +196,14 @@ def sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms):
     rc = load().sgemm_plan(M, N, K, lda, ldb, ldc, a_addr, b_addr, c_addr, num_sms,
                            ctypes.byref(cfg), ctypes.byref(pa), ctypes.byref(pb))
     return rc, cfg.value, pa.value, pb.value
+
+
+def sgemm_plan_row_tail(config, M, N, K, batch=1):
+    """Host-only: (status, rows) — the last rows of C that a call on this
+    configuration computes with the row-tail kernel (0: none)."""
+    rows = ctypes.c_int64(-1)
+    rc = load().sgemm_plan_row_tail(config, M, N, K, batch, ctypes.addressof(rows))
+    return rc, rows.value
 
 
 def sgemm_general_plan(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b, beta, ldc, stride_c,

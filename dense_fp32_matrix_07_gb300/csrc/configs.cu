@@ -79,6 +79,19 @@ int select_config(const ProblemShape &p)
     return kCfgFfma2_128x64;
 }
 
+int64_t row_tail_rows(int cfg, int64_t M, int64_t N, int64_t K, int64_t batch)
+{
+    if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].packs || batch < 1 || batch > 65535) return 0;
+    const int64_t bm = kConfigTable[cfg].bm, bn = kConfigTable[cfg].bn;
+    const int64_t r = M % bm;
+    if (r < 1 || r > kRowTailMax || M <= bm) return 0;
+    // The padded block row costs round_up(N, bn) * bm * K FMAs of the tiled
+    // product; from about 2.7e8 of them (some 7 us) the tail kernel, which
+    // streams B once in a few microseconds, is the cheaper way.
+    if ((double)((N + bn - 1) / bn * bn) * (double)K < 2097152.0) return 0;
+    return r;
+}
+
 size_t config_workspace_bytes(int cfg, const GemmArgs &g)
 {
     if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].uses_tma) return 0;

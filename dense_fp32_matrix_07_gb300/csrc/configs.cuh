@@ -106,6 +106,30 @@ cudaError_t prepare_ffma_tma_ktail();
 // Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
 cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);
 
+// The last r <= kRowTailMax rows of C of a product whose tiled part covers
+// rows 0 .. m0 - 1 (kernels_row_tail.cu): C_b[m0 + i][j] = alpha * sum_k
+// op(A_b)[m0 + i][k] * B_b[k][j] (+ beta * C_b[m0 + i][j] when beta != 0).
+constexpr int kRowTailMax = 8;
+struct RowTailArgs {
+    const float *A;      // op(A_b)[m][k] at A + b * stride_a + m * a_row_stride + k * a_k_stride
+    int64_t a_row_stride, a_k_stride, stride_a;
+    const float *B;      // B_b: K x N row-major, ldb, rows 16-byte aligned (the TMA path's B)
+    int64_t ldb, stride_b;
+    float *C;
+    int64_t ldc, stride_c;
+    int64_t m0;          // first row of the tail
+    int r;               // rows, 1 .. kRowTailMax
+    int64_t N, K, batch;
+    float alpha, beta;
+};
+cudaError_t launch_row_tail(const RowTailArgs &t, int num_sms, cudaStream_t stream);
+
+// Rows that a call with this configuration leaves to the row-tail kernel:
+// M = 128 q + r with 1 <= r <= kRowTailMax on a TMA FFMA configuration, when
+// the block row of tiles those rows would pad is worth more than the tail
+// kernel's fixed cost (round_up(N, BN) * K >= 2^21); else 0.
+int64_t row_tail_rows(int cfg, int64_t M, int64_t N, int64_t K, int64_t batch);
+
 // The 3xTF32 tensor-core path (kernels_tf32x3.cu): split pre-passes into
 // g.workspace, then the tcgen05 product.
 cudaError_t launch_tf32x3(int kernel, const GemmArgs &g, cudaStream_t stream);

@@ -162,6 +162,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
             ptx::mbar_init(empty_bar(s), Cfg::CONSUMERS);
         }
         ptx::mbar_init_fence();
+        // A kernel queued behind this one with programmatic serialization
+        // (the last-rows kernel, which reads nothing this grid writes) may
+        // take SMs as soon as this persistent grid's CTAs leave them.
+        ptx::grid_launch_dependents();
     }
     __syncthreads();
 

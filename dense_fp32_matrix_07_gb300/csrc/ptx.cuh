@@ -143,6 +143,22 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
         : "memory");
 }
 
+// Programmatic dependent launch: lets the next kernel of the stream, when
+// it was launched with programmatic stream serialization, be scheduled
+// before this grid completes (once every CTA has signalled or exited).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on programmatically have completed
+// and their memory operations are visible (returns at once without such a
+// dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Rank of this CTA in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -164,6 +180,21 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16 bytes at shared-memory offset `addr` of the cluster's CTA `rank`
+// (distributed shared memory; the peer must keep that memory alive, e.g. by
+// a cluster barrier after the read).
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr, uint32_t rank)
+{
+    float4 v;
+    asm volatile("{\n\t.reg .b32 ra;\n\t"
+                 "mapa.shared::cluster.u32 ra, %4, %5;\n\t"
+                 "ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [ra];\n\t}"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr), "r"(rank)
+                 : "memory");
+    return v;
 }
 
 // One arrival on the mbarrier at offset `bar` of the cluster's CTA `rank`.

@@ -303,7 +303,6 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     if (rc == kNothingToDo) return SGEMM_OK;
     if (rc != SGEMM_OK) return rc;
     const bool reads_ab = c.K > 0 && c.alpha != 0.0f;
-    const int64_t a_rows = c.op_a ? c.K : c.M, a_cols = c.op_a ? c.M : c.K;
 
     DeviceState *dev = nullptr;
     rc = device_state(&dev);
@@ -324,7 +323,14 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     rc = plan_call(c, dev->num_sms, &cfg, &pa, &pb);
     if (rc != SGEMM_OK) return rc;
 
-    GemmArgs g{c.M, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
+    // The last `tail` rows (M just past a multiple of the block height) go
+    // to the row-tail kernel; the tiled product covers the first Mm rows.
+    const int64_t tail = row_tail_rows(cfg, c.M, c.N, c.K, c.batch);
+    const int64_t Mm = c.M - tail;
+    // Stored shape of the part of A the tiled product reads.
+    const int64_t a_rows = c.op_a ? c.K : Mm, a_cols = c.op_a ? Mm : c.K;
+
+    GemmArgs g{Mm, c.N, c.K, c.A, c.lda, c.B, c.ldb, c.C, c.ldc, dev->status, dev->num_sms};
     g.sched = c.sched_override >= 0 ? c.sched_override : kConfigTable[cfg].sched;
     g.withhold_it = c.withhold_it;
     g.alpha = c.alpha;
@@ -337,8 +343,8 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     g.op_b = c.op_b;
 
     const bool akm = kConfigTable[cfg].a_kmajor;
-    const int64_t a_rows_p = akm ? c.K : c.M;                       // rows of the packed A
-    const int64_t lda_p = round_up(akm ? c.M : c.K, 32), ldb_p = round_up(c.N, 32);
+    const int64_t a_rows_p = akm ? c.K : Mm;                        // rows of the packed A
+    const int64_t lda_p = round_up(akm ? Mm : c.K, 32), ldb_p = round_up(c.N, 32);
     const int64_t a_entries = (c.batch > 1 && c.sa != 0) ? c.batch : 1;
     const int64_t b_entries = (c.batch > 1 && c.sb != 0) ? c.batch : 1;
     const size_t a_bytes = pa ? (size_t)(a_entries * a_rows_p * lda_p) * 4 : 0;
@@ -396,7 +402,29 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
         }
     }
 
-    const cudaError_t err = launch_config(cfg, g, stream);
+    cudaError_t err = launch_config(cfg, g, stream);
+    if (err == cudaSuccess && tail > 0) {
+        // The tail rows, from the caller's A and the B the product read.
+        RowTailArgs t{};
+        t.A = c.A;
+        t.a_row_stride = c.op_a ? 1 : c.lda;
+        t.a_k_stride = c.op_a ? c.lda : 1;
+        t.stride_a = c.batch > 1 ? c.sa : 0;
+        t.B = g.B;
+        t.ldb = g.ldb;
+        t.stride_b = g.stride_b;
+        t.C = c.C;
+        t.ldc = c.ldc;
+        t.stride_c = c.batch > 1 ? c.sc : 0;
+        t.m0 = Mm;
+        t.r = (int)tail;
+        t.N = c.N;
+        t.K = c.K;
+        t.batch = c.batch;
+        t.alpha = c.alpha;
+        t.beta = c.beta;
+        err = launch_row_tail(t, dev->num_sms, stream);
+    }
     if (scratch) cudaFreeAsync(scratch, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -530,6 +558,15 @@ int sgemm_general_plan(int op_a, int op_b, int64_t M, int64_t N, int64_t K, floa
     if (out_config) *out_config = cfg;
     if (out_pack_a) *out_pack_a = pa ? 1 : 0;
     if (out_pack_b) *out_pack_b = pb ? 1 : 0;
+    return SGEMM_OK;
+}
+
+int sgemm_plan_row_tail(int config, int64_t M, int64_t N, int64_t K, int64_t batch, int64_t *out_rows)
+{
+    if (!out_rows) return SGEMM_ERR_INVALID_VALUE;
+    *out_rows = 0;
+    if (config < 0 || config >= kNumConfigs || M < 0 || N < 0 || K < 0 || batch < 0) return SGEMM_ERR_INVALID_VALUE;
+    *out_rows = row_tail_rows(config, M, N, K, batch);
     return SGEMM_OK;
 }
 

@@ -35,9 +35,10 @@
  * memory pool on `stream` and returned on `stream`; it is never exposed.
  * Asynchrony: calls return after enqueueing work on `stream`; results are
  * ready when the stream's work completes. An FFMA call enqueues at most
- * three kernels (operand packing, then the product) plus a memset of the
- * stream-K arrival counters; a 3xTF32 call enqueues two split passes and
- * the product per batch entry. No call synchronises the host.
+ * four kernels (operand packing, the product, and the kernel of the last
+ * rows that sgemm_plan_row_tail() describes) plus a memset of the stream-K
+ * arrival counters; a 3xTF32 call enqueues two split passes and the
+ * product per batch entry. No call synchronises the host.
  * Graph capture: sgemm(), sgemm_ex(), sgemm_general() and sgemm_general_ex()
  * may be captured into a CUDA graph once one call has run on the device
  * (the first call sets the device up); a replay computes the product of
@@ -57,9 +58,11 @@ extern "C" {
 /* Status codes. A nonzero code returned by a call means that C is untouched:
  * argument errors return before anything is enqueued; a failing launch may
  * follow scratch-only work (an operand pack, a TF32 split) already enqueued
- * on the stream. One exception: in a batched call on a 3xTF32 configuration,
- * which launches entry after entry, a launch that fails at entry b leaves
- * entries 0 .. b-1 computed. */
+ * on the stream. Two exceptions: in a batched call on a 3xTF32
+ * configuration, which launches entry after entry, a launch that fails at
+ * entry b leaves entries 0 .. b-1 computed; and when the launch of the
+ * last-rows kernel (sgemm_plan_row_tail()) fails, the product of the other
+ * rows has been enqueued. */
 enum {
     SGEMM_OK = 0,
     SGEMM_ERR_INVALID_VALUE = 1, /* negative size, short leading dimension,
@@ -248,6 +251,27 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K,
                uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
                int num_sms,
                int *out_config, int *out_pack_a, int *out_pack_b);
+
+/*
+ * sgemm_plan_row_tail — host-only, needs no GPU: how many of the last rows
+ * of C a call computes apart from its tiled product.
+ *
+ * The TMA configurations tile C in 128-row block rows. When M = 128 q + r
+ * with 1 <= r <= 8 (M > 128) and the block row those r rows would pad is
+ * large (round_up(N, tile width) * K >= 2^21), the call runs the tiled
+ * product on the first M - r rows and a small kernel on the last r: each of
+ * those rows is the dot product of a row of A with every column of B, as
+ * the course page "Перемножение матриц: наивное и тайловое", section 1,
+ * defines C, computed by clusters of CTAs that split K and add their parts
+ * in a fixed order. Arguments: `config`, the configuration the call runs
+ * (from sgemm_plan() or sgemm_general_plan(), or a forced one); M, N, K and
+ * `batch` of the call. *out_rows receives r, or 0 when the call has no such
+ * kernel (which adds one launch when it runs). Returns SGEMM_OK, or
+ * SGEMM_ERR_INVALID_VALUE for an unknown config, a negative size or a NULL
+ * out_rows.
+ */
+int sgemm_plan_row_tail(int config, int64_t M, int64_t N, int64_t K, int64_t batch,
+                        int64_t *out_rows);
 
 /*
  * sgemm_test_withhold_copy — test hook for the device-side wait limit.

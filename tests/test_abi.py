@@ -172,3 +172,33 @@ def test_general_plan_follows_the_library_choice():
     ladder = sg.config_ids()["ladder_register_tiled_2x2"]
     assert plan(0, 0, 256, 256, 256, 1.0, 256, 0, 256, 0, 0.5, 256, 0, 1, config=ladder)[0] == \
         sg.SGEMM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M,N,K,rows", [
+    (4097, 3001, 2049, 1),      # the odd rectangle: one row past 32 block rows
+    (4100, 3001, 2049, 4),
+    (4104, 3001, 2049, 8),
+    (4105, 3001, 2049, 0),      # 9 rows: the tiled product pads them
+    (4096, 4096, 4096, 0),      # whole block rows
+    (129, 129, 129, 0),         # M not past a block row, and a small product
+    (1025, 1024, 1024, 0),      # round_up(N, BN) * K = 2^20: below the tail kernel's fixed cost
+    (1025, 1024, 2048, 1),
+])
+def test_row_tail_decision(M, N, K, rows):
+    rc, cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, 152)
+    assert rc == 0
+    assert sg.sgemm_plan_row_tail(cfg, M, N, K) == (0, rows)
+
+
+def test_row_tail_only_on_tma_ffma_configurations():
+    ids = sg.config_ids()
+    for name in ("tiled16_simple", "ladder_register_tiled_2x2", "tf32x3_128x256_k16_s4", "tf32x3_pair_128x256_k16_s4"):
+        assert sg.sgemm_plan_row_tail(ids[name], 4097, 3001, 2049) == (0, 0), name
+    for name in ("ffma2_128x256_k32_s4", "ffma2_128x128_k32_s4_ka", "ffma2_128x64_k32_s4", "ffma_128x128_k32_s4"):
+        assert sg.sgemm_plan_row_tail(ids[name], 4097, 3001, 2049) == (0, 1), name
+    # Batches of up to 65535 entries (one grid dimension of the tail kernel).
+    cfg = ids["ffma2_128x256_k32_s4"]
+    assert sg.sgemm_plan_row_tail(cfg, 4097, 3001, 2049, 65535) == (0, 1)
+    assert sg.sgemm_plan_row_tail(cfg, 4097, 3001, 2049, 65536) == (0, 0)
+    assert sg.sgemm_plan_row_tail(-1, 4097, 3001, 2049)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.sgemm_plan_row_tail(cfg, -1, 3001, 2049)[0] == sg.SGEMM_ERR_INVALID_VALUE
