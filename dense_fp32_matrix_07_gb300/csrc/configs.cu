@@ -71,6 +71,13 @@ int select_config(const ProblemShape &p)
     // against k-major: 2048 x 2048 x 512 81.6 against 85.7 us, 1536 x 2048 x
     // 2048 212.6 against 212.7 us, 2048^3 276.1 against 274.1 us).
     const bool kmajor = p.N >= 2048 && (double)p.M * (double)p.N * (double)p.K >= 6.0e9;
+    // With A k-major, the 128 x 128 tiles keep up with the 128 x 256 ones
+    // and even out the last waves better while the 128 x 256 grid spans
+    // under three waves (same-box A/B, 128 x 128 against 128 x 256:
+    // 4097 x 3001 x 2049 789.0 against 798.1 us, 3072^3 849.7 against 854.1
+    // us, 4096^3 (3.4 waves) 1975.1 against 1975.9 us, 6144^3 (7.6 waves)
+    // 6586.5 against 6578.8 us).
+    if (kmajor && tiles256 >= p.num_sms && tiles256 < 3 * (int64_t)p.num_sms) return kCfgFfma2_128x128_ka;
     if (tiles256 >= p.num_sms) return kmajor ? kCfgFfma2_128x256_ka : kCfgFfma2_128x256;
     // The 128x128 block's k-major twin by the same rule (8x8 loop alone 89.5 %
     // against 86.0 %; same-box sweep: 2048^3 78.3 % against 77.3 %, 2048 x

@@ -114,9 +114,14 @@ def test_schedule_invariants_random():
 
 
 def test_auto_policy_choices():
-    # 4096^3 on 128x256 tiles: two whole-tile waves, the last 1.37 waves stream-K.
+    # 4096^3 on 128x256 tiles: three whole-tile waves, then stream-K over the
+    # 56 leftover tiles (at least a third of the 152 slots).
     _, info = sg.sgemm_test_schedule(4096, 4096, 4096, 128, 256, 32, 152, AUTO)
-    assert info["dp_tiles"] == 304 and info["sk_ctas"] == 152
+    assert info["dp_tiles"] == 456 and info["sk_ctas"] == 152
+    # 4096 x 3001 x 2049 on 128x128 tiles: 8 leftover tiles are under a third
+    # of the slots, so the last full wave joins the stream-K region.
+    _, info = sg.sgemm_test_schedule(4096, 3001, 2049, 128, 128, 32, 152, AUTO)
+    assert info["dp_tiles"] == 4 * 152 and info["sk_ctas"] == 152
     # 16384^3: the last wave is 99.8 % full, so whole tiles only.
     _, info = sg.sgemm_test_schedule(16384, 16384, 16384, 128, 256, 32, 152, AUTO)
     assert info["sk_ctas"] == 0 and info["dp_tiles"] == info["tiles"]
@@ -124,7 +129,7 @@ def test_auto_policy_choices():
     _, info = sg.sgemm_test_schedule(1536, 1536, 1536, 128, 128, 32, 152, AUTO)
     assert info["sk_ctas"] == 0
     # 8192^3 on 128x256 tiles: 13.47 waves, 96.2 % of the slots busy under
-    # whole tiles; after a full wave that is evened out: 12 whole-tile waves,
-    # then stream-K over the last 200 tiles.
+    # whole tiles; after a full wave that is evened out: 13 whole-tile waves,
+    # then stream-K over the 72 leftover tiles.
     _, info = sg.sgemm_test_schedule(8192, 8192, 8192, 128, 256, 32, 152, AUTO)
-    assert info["dp_tiles"] == 12 * 152 and info["sk_ctas"] == 152
+    assert info["dp_tiles"] == 13 * 152 and info["sk_ctas"] == 152
