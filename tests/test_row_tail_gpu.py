@@ -95,3 +95,19 @@ def test_row_tail_in_the_general_form(cuda_device, oracle, op_a, op_b, alpha, be
         want = alpha * Cref + beta * C0[b].double().numpy()
         # Integer inputs, alpha and beta exact in FP32: the result is exact.
         assert_parity(C[b], want, S, True, f"entry {b}")
+
+
+@pytest.mark.parametrize("M,N,K", [(131, 300, 8000), (4097, 1024, 20000), (261, 2000, 12345)])
+def test_row_tail_with_k_split_across_a_cluster(cuda_device, oracle, M, N, K):
+    # Few column blocks, or a long K: clusters of 8 CTAs split K and rank 0
+    # adds their sums through distributed shared memory.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rc, cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, sms)
+    assert rc == 0 and _tail_rows(cfg, M, N, K) == M % 128
+    for dist, exact in (("normal", False), ("int", True)):
+        A, B = workloads.make_operands(M, N, K, dist, 21)
+        rc, C, dC = run(M, N, K, A, K, B, N)
+        assert rc == 0
+        Cref, S = oracle.sgemm(M, N, K, A.numpy(), K, B.numpy(), N)
+        assert_parity(C, Cref, S, exact, f"{M}x{N}x{K} {dist}")
+        check_untouched_padding(dC, N)
