@@ -16,7 +16,7 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"ffma2_128x256_k32_s4_sk", kKernFfma2_128x256k32s4, kSchedStreamK, true, true, 128, 256},
     {"ladder_naive_rowmap", kKernLadderNaive, kSchedDataParallel, false, false, 16, 16},
     {"ladder_coalesced", kKernLadderCoalesced, kSchedDataParallel, false, false, 16, 16},
-    {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, false, 128, 128},
+    {"ladder_cache_blocked_8x8", kKernLadderCacheBlocked8x8, kSchedDataParallel, false, false, 8, 8},
     {"ladder_register_tiled_2x2", kKernLadderRegisterTiled2x2, kSchedDataParallel, false, false, 16, 16},
     {"tf32x3_128x256_k16_s4", kKernTf32x3_128x256, kSchedTailSplit, true, false, 128, 256},
     {"tf32x3_128x256_k16_s4_sk", kKernTf32x3_128x256, kSchedStreamK, true, false, 128, 256},

@@ -39,42 +39,54 @@ __global__ void ladder_coalesced_kernel(int64_t M, int64_t N, int64_t K, const f
     C[i * ldc + j] = sum;
 }
 
-// The CUDA Handbook, ch.17, section 17.3 (Cache Blocking): each thread owns a
-// TM x TN micro-tile of C in registers, walks K one step at a time loading TM
-// values of A and TN of B, and no shared memory is used — the L1/L2 caches
-// capture the reuse between neighbouring threads. Grid-stride loops over
-// micro-tiles as on the page; the store the page elides is written out.
+// The CUDA Handbook, ch.17, section 17.3 (Cache Blocking), as a design: a
+// thread computes a TM x TN block of C wholly in registers, reading A and B
+// straight from global memory without shared memory, and the caches capture
+// the reuse: threads of a warp take side-by-side blocks, so their B reads
+// share cache lines and their A values are the same few rows. Here the
+// blocks are dealt out by one flat index over a 1-D grid, consecutive
+// indices running along a row of blocks; rows and columns past the edge of
+// C are clamped to the last valid ones while reading and skipped when
+// storing, so no load needs a predicate.
 template <int TM, int TN>
-__global__ void ladder_cache_blocked_kernel(int64_t M, int64_t N, int64_t K,
-                                            const float *__restrict__ A, int64_t lda,
-                                            const float *__restrict__ B, int64_t ldb,
-                                            float *__restrict__ C, int64_t ldc)
+__global__ void __launch_bounds__(256)
+ladder_cache_blocked_kernel(int64_t M, int64_t N, int64_t K, const float *__restrict__ A, int64_t lda,
+                            const float *__restrict__ B, int64_t ldb, float *__restrict__ C, int64_t ldc)
 {
-    for (int64_t row0 = (blockIdx.y * (int64_t)blockDim.y + threadIdx.y) * TM; row0 < M;
-         row0 += (int64_t)gridDim.y * blockDim.y * TM) {
-        for (int64_t col0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * TN; col0 < N;
-             col0 += (int64_t)gridDim.x * blockDim.x * TN) {
-            float acc[TM][TN];
+    const int64_t blocks_n = (N + TN - 1) / TN;
+    const int64_t blocks = ((M + TM - 1) / TM) * blocks_n;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < blocks; blk += step) {
+        const int64_t r0 = (blk / blocks_n) * TM, c0 = (blk % blocks_n) * TN;
+        int64_t arow[TM], bcol[TN];
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < TM; ++i) arow[i] = (r0 + i < M ? r0 + i : M - 1) * lda;
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-            for (int64_t k = 0; k < K; ++k) {
-                float a[TM], b[TN];
+        for (int j = 0; j < TN; ++j) bcol[j] = c0 + j < N ? c0 + j : N - 1;
+        float acc[TM][TN];
 #pragma unroll
-                for (int i = 0; i < TM; ++i) a[i] = row0 + i < M ? A[(row0 + i) * lda + k] : 0.0f;
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) b[j] = col0 + j < N ? B[k * ldb + col0 + j] : 0.0f;
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        const float *bk = B;
+        for (int64_t k = 0; k < K; ++k, bk += ldb) {
+            float bv[TN];
 #pragma unroll
-                for (int i = 0; i < TM; ++i)
+            for (int j = 0; j < TN; ++j) bv[j] = bk[bcol[j]];
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            for (int i = 0; i < TM; ++i) {
+                const float av = A[arow[i] + k];
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
             }
+        }
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < TM; ++i) {
+            if (r0 + i >= M) break;
+            float *crow = C + (r0 + i) * ldc;
 #pragma unroll
-                for (int j = 0; j < TN; ++j)
-                    if (row0 + i < M && col0 + j < N) C[(row0 + i) * ldc + col0 + j] = acc[i][j];
+            for (int j = 0; j < TN; ++j)
+                if (c0 + j < N) crow[c0 + j] = acc[i][j];
         }
     }
 }
@@ -167,10 +179,11 @@ cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream)
         break;
     }
     case kKernLadderCacheBlocked8x8: {
-        const dim3 block(16, 16);
-        const int64_t gx = clamp_grid((g.N + 127) / 128, 4096), gy = clamp_grid((g.M + 127) / 128, 4096);
-        ladder_cache_blocked_kernel<8, 8><<<dim3((unsigned)gx, (unsigned)gy), block, 0, stream>>>(
-            g.M, g.N, g.K, g.A, g.lda, g.B, g.ldb, g.C, g.ldc);
+        // One 8 x 8 block of C per thread, 256 threads a CTA, at most 16
+        // CTAs per SM's worth of blocks at once (grid-stride beyond that).
+        const int64_t blocks = ((g.M + 7) / 8) * ((g.N + 7) / 8);
+        ladder_cache_blocked_kernel<8, 8><<<clamp_grid((blocks + 255) / 256, (int64_t)g.num_sms * 16), 256, 0,
+                                            stream>>>(g.M, g.N, g.K, g.A, g.lda, g.B, g.ldb, g.C, g.ldc);
         break;
     }
     case kKernLadderRegisterTiled2x2: {
