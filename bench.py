@@ -541,7 +541,7 @@ def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_i
             "fp32_peak_pct": round(100.0 * value / 1e3 / peak_tflops, 2),
             "best_step_fp32_peak_pct": round(100.0 * best / 1e3 / peak_tflops, 2),
             "steps": len(ms),
-            "launches_per_step": 1 + pa + pb + (1 if sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1] > 0 else 0),
+            "launches_per_step": 1 + (1 if pa or pb else 0) + (1 if sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1] > 0 else 0),
             "step_ms": {"median": round(statistics.median(ms), 4), "best": round(min(ms), 4),
                         "mean": round(statistics.mean(ms), 4)},
             "l2": l2,
@@ -643,10 +643,15 @@ def run_ours(args, local, extra):
             if w.K * r32(w.M) + (w.K * r32(w.N) if pb else 0) > (16 << 20):
                 cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
                 pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
-        # The packs, the product and, for an M just past a multiple of the
-        # block height, the kernel of the last rows (sgemm_noalloc has none).
+        # The operand layout pass (one launch for both operands; sgemm_noalloc
+        # launches one per operand), the product and, for an M just past a
+        # multiple of the block height, the kernel of the last rows
+        # (sgemm_noalloc has none).
         tail = 0 if args.noalloc else sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1]
-        launches_per_step = 1 + pa + pb + (1 if tail > 0 else 0)
+        packs = pa + pb if args.noalloc else (1 if pa or pb else 0)
+        launches_per_step = 1 + packs + (1 if tail > 0 else 0)
+        other_launches = ([f"{packs} operand layout pass(es)"] if packs else []) + \
+            (["the last-rows kernel"] if tail > 0 else [])
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
         flops = product_flops(w.M, w.N, w.K)
 
@@ -678,7 +683,10 @@ def run_ours(args, local, extra):
             raise SystemExit(f"general form: {sg.sgemm_error_string(rc)}")
         packs = sg.sgemm_config_name(cfg).startswith("ffma")
         tail = sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K, args.batch)[1]
-        launches_per_step = (1 + pa + pb + (1 if tail > 0 else 0)) if packs else 3 * args.batch
+        launches_per_step = (1 + (1 if pa or pb else 0) + (1 if tail > 0 else 0)) if packs else 3 * args.batch
+        other_launches = ((["the operand layout pass"] if pa or pb else []) +
+                          (["the last-rows kernel"] if tail > 0 else [])) if packs else \
+            [f"{2 * args.batch} 3xTF32 split passes ({args.batch} entries, one product launch each)"]
         total_bytes = 4 * args.batch * (sa + sb + sc)
         flops = args.batch * product_flops(w.M, w.N, w.K)
 
@@ -905,9 +913,8 @@ def run_ours(args, local, extra):
                      "peak_basis": f"{num_sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
                                    f"{sm_max:.0f} MHz (max SM clock)",
                      "achieved_basis": ("2MNK / mean CUDA-event time of one call: the product kernel"
-                                        + (f" with {launches_per_step - 1} other launch(es): operand "
-                                           "packs and the last-rows kernel"
-                                           if launches_per_step > 1 else "")
+                                        + (" with " + " and ".join(other_launches)
+                                           if other_launches else "")
                                         + ", on the launching stream")},
         "clocks": clocks,
         "host_elapsed_s": round(elapsed_host, 3),

@@ -39,6 +39,12 @@ struct GemmArgs {
     // (A stored K x M, B stored N x K). Only kernels that read the operands
     // themselves (the 3xTF32 split) see 1; the others get packed copies.
     int op_a = 0, op_b = 0;
+    // Set when this call's layout pass (launch_pack_pair) was queued right
+    // before the product and has zeroed the stream-K arrival counters at the
+    // start of `workspace`: the product then skips its own zeroing and
+    // launches with programmatic stream serialization, its CTAs waiting for
+    // the pass to complete before they touch memory.
+    bool behind_pack = false;
 };
 
 // Bits of the device error word.
@@ -59,15 +65,25 @@ cudaError_t device_status_word(unsigned int **out);
 // Launchers (each returns the launch's cudaGetLastError()).
 cudaError_t launch_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc,
                              cudaStream_t stream);
-cudaError_t launch_pack(const float *src, int64_t rows, int64_t cols,
-                        int64_t ld_src, float *dst, int64_t ld_dst,
-                        cudaStream_t stream);
-// Batched copies: entry b of src (rows x cols, ld_src, batch stride
-// s_src) to dst (ld_dst, batch stride s_dst); the transposing variant
-// writes dst[b][c][r] = src[b][r][c].
-cudaError_t launch_pack_batched(const float *src, int64_t rows, int64_t cols, int64_t ld_src,
-                                int64_t s_src, float *dst, int64_t ld_dst, int64_t s_dst,
-                                int64_t batch, cudaStream_t stream);
+// One operand's layout pass: entry b of src (rows x cols, ld_src, batch
+// stride s_src) to dst (ld_dst, batch stride s_dst), copied as it is or
+// transposed (dst[b][c][r] = src[b][r][c]), by `blocks` blocks of 256 threads.
+struct PackJob {
+    const float *src;
+    int64_t rows, cols, ld_src, s_src;
+    float *dst;
+    int64_t ld_dst, s_dst, batch;
+    int transpose;
+    int64_t blocks;
+};
+PackJob pack_job(const float *src, int64_t rows, int64_t cols, int64_t ld_src, int64_t s_src, float *dst,
+                 int64_t ld_dst, int64_t s_dst, int64_t batch, bool transpose);
+// Jobs a and b (either may have 0 blocks) in one launch, which also zeroes
+// zero_bytes at `zero` (null: nothing) and lets a kernel queued behind it with
+// programmatic stream serialization start while its last blocks run.
+cudaError_t launch_pack_pair(const PackJob &a, const PackJob &b, unsigned int *zero, size_t zero_bytes,
+                             cudaStream_t stream);
+// One transposing layout pass on its own (the allocation-free entry point).
 cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_t cols,
                                           int64_t ld_src, int64_t s_src, float *dst,
                                           int64_t ld_dst, int64_t s_dst, int64_t batch,

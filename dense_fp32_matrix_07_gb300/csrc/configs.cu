@@ -112,6 +112,14 @@ size_t config_workspace_bytes(int cfg, const GemmArgs &g)
     return ffma_tma_workspace_bytes(kConfigTable[cfg].kernel, a);
 }
 
+size_t config_counter_bytes(int cfg, const GemmArgs &g)
+{
+    if (cfg < 0 || cfg >= kNumConfigs || !kConfigTable[cfg].packs) return 0;
+    GemmArgs a = g;
+    if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
+    return ffma_tma_counter_bytes(kConfigTable[cfg].kernel, a);
+}
+
 cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
     const int kernel = kConfigTable[cfg].kernel;

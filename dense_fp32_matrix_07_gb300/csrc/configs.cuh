@@ -83,6 +83,9 @@ bool config_supports(int cfg, const ProblemShape &p);
 
 // Workspace bytes configuration `cfg` wants for this product (0: none).
 size_t config_workspace_bytes(int cfg, const GemmArgs &g);
+// For an FFMA TMA configuration given g.workspace_bytes: the bytes at the
+// start of the workspace that must be zero when the product starts (0: none).
+size_t config_counter_bytes(int cfg, const GemmArgs &g);
 
 // Runs configuration `cfg` on operands that already satisfy its alignment
 // needs (the API packs misaligned operands for TMA configurations first).
@@ -97,6 +100,7 @@ cudaError_t configs_prepare_device();
 // Launchers of the TMA kernels (kernels_ffma_tma.cu), by KernelId.
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream);
 size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g);
+size_t ffma_tma_counter_bytes(int kernel, const GemmArgs &g);
 cudaError_t prepare_ffma_tma();
 // The same kernels trimming the last K slab, for K not a multiple of the
 // slab depth (kernels_ffma_tma_ktail.cu); launch_ffma_tma() dispatches there.

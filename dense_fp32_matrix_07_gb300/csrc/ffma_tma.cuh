@@ -168,6 +168,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         ptx::grid_launch_dependents();
     }
     __syncthreads();
+    // Queued behind the call's layout pass with programmatic serialization,
+    // this grid may start while that pass still runs: no thread touches
+    // global memory before the pass has completed (a no-op otherwise).
+    ptx::grid_dependency_wait();
 
     if (warp >= Cfg::CONSUMERS) {
         // ------------------------------ producer ------------------------------
@@ -574,6 +578,16 @@ size_t workspace_bytes(const Schedule &s)
     return schedule_workspace_bytes(s, Cfg::CONSUMERS, Cfg::BM, Cfg::BN);
 }
 
+// Bytes at the start of the workspace that must be zero when the product
+// starts (its stream-K arrival counters; 0 for whole tiles).
+template <class Cfg>
+size_t counter_bytes(const GemmArgs &g)
+{
+    if (g.workspace == nullptr) return 0;
+    const Schedule s = make_schedule<Cfg>(g, true);
+    return g.workspace_bytes >= workspace_bytes<Cfg>(s) ? schedule_counter_bytes(s, Cfg::CONSUMERS) : 0;
+}
+
 // Launches the product; K_TAIL selects the kernel that trims the last slab
 // (for K not a multiple of BK).
 template <class Cfg, bool K_TAIL>
@@ -596,7 +610,8 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     // Stream-K needs the caller's workspace; without one the schedule is whole tiles.
     Schedule s = make_schedule<Cfg>(g, g.workspace != nullptr);
     if (s.sk_ctas > 0 && g.workspace_bytes < workspace_bytes<Cfg>(s)) s = make_schedule<Cfg>(g, false);
-    if (s.sk_ctas > 0 && (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, stream)) != cudaSuccess)
+    if (s.sk_ctas > 0 &&
+        (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, !g.behind_pack, stream)) != cudaSuccess)
         return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0) &&
                      (g.batch <= 1 || g.stride_c % 4 == 0);
@@ -607,8 +622,23 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true, K_TAIL>)
                          : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false, K_TAIL>);
     // No CTA waits for another (split tiles are reduced by their last part),
-    // so this is an ordinary launch.
-    e = cudaLaunchKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    // so this is an ordinary launch; behind the call's layout pass it may
+    // start early (programmatic serialization), its CTAs waiting for the pass.
+    if (g.behind_pack) {
+        cudaLaunchConfig_t lc = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.gridDim = dim3(s.grid);
+        lc.blockDim = dim3(Cfg::THREADS);
+        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        lc.stream = stream;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        e = cudaLaunchKernelExC(&lc, fn, args);
+    } else {
+        e = cudaLaunchKernel(fn, dim3(s.grid), dim3(Cfg::THREADS), args, Cfg::SMEM_BYTES, stream);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 // shape, stride and alignment), the zero fill used when K == 0, and the
 // operand pack that gives misaligned operands 16-byte-aligned rows.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace sgemm_gb300 {
 
@@ -83,99 +84,63 @@ cudaError_t launch_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc,
 }
 
 // ---------------------------------------------------------------------------
-// Pack: dst[r * ld_dst + c] = src[r * ld_src + c] for r < rows, c < cols.
-// Each warp copies one row segment per iteration, so both the 4-byte reads
-// (of a possibly misaligned source) and the writes are coalesced. Entries of
-// dst beyond `cols` are left as they are: the product never reads them (its
-// tensor maps describe only `cols` columns and fill the rest with zero).
-// ---------------------------------------------------------------------------
-__global__ void pack_kernel(const float *__restrict__ src, int64_t rows,
-                            int64_t cols, int64_t ld_src,
-                            float *__restrict__ dst, int64_t ld_dst)
-{
-    const int64_t segs = (cols + 255) / 256;       // 256-column segments per row
-    const int64_t work = rows * segs;
-    const int warps = blockDim.x / 32;
-    const int lane = threadIdx.x & 31;
-    for (int64_t w = blockIdx.x * (int64_t)warps + threadIdx.x / 32; w < work;
-         w += (int64_t)gridDim.x * warps) {
-        const int64_t r = w / segs;
-        const int64_t c0 = (w % segs) * 256;
-        const float *s = src + r * ld_src;
-        float *d = dst + r * ld_dst;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int64_t c = c0 + q * 32 + lane;
-            if (c < cols) d[c] = s[c];
-        }
-    }
-}
-
-cudaError_t launch_pack(const float *src, int64_t rows, int64_t cols,
-                        int64_t ld_src, float *dst, int64_t ld_dst,
-                        cudaStream_t stream)
-{
-    const int64_t work = rows * ((cols + 255) / 256);
-    int64_t blocks = (work + 7) / 8;
-    if (blocks > 8192) blocks = 8192;
-    if (blocks < 1) blocks = 1;
-    pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, rows, cols, ld_src,
-                                                     dst, ld_dst);
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
 // Batched layout kernels of the general form alpha * op(A) . op(B) + beta * C.
 // ---------------------------------------------------------------------------
 
-// dst[b * s_dst + r * ld_dst + c] = src[b * s_src + r * ld_src + c].
-__global__ void pack_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
-                                    int64_t ld_src, int64_t s_src, float *__restrict__ dst,
-                                    int64_t ld_dst, int64_t s_dst, int64_t batch)
+// dst[b * s_dst + r * ld_dst + c] = src[b * s_src + r * ld_src + c]: each
+// warp copies 256-column segments of rows, block `blk` of `nblk` (256
+// threads) taking every nblk-th group of 8 segments, so the 4-byte reads (of
+// a possibly misaligned source) and the writes are coalesced. Entries of dst
+// beyond `cols` are left as they are: the product never reads them (its
+// tensor maps describe only `cols` columns and fill the rest with zero).
+__device__ __forceinline__ void copy_rows(const PackJob &j, int64_t blk, int64_t nblk)
 {
-    const int64_t segs = (cols + 255) / 256;
-    const int64_t work = batch * rows * segs;
-    const int warps = blockDim.x / 32;
+    const int64_t segs = (j.cols + 255) / 256;
+    const int64_t work = j.batch * j.rows * segs;
     const int lane = threadIdx.x & 31;
-    for (int64_t w = blockIdx.x * (int64_t)warps + threadIdx.x / 32; w < work;
-         w += (int64_t)gridDim.x * warps) {
+    for (int64_t w = blk * 8 + threadIdx.x / 32; w < work; w += nblk * 8) {
         const int64_t seg = w % segs, rb = w / segs;
-        const int64_t r = rb % rows, b = rb / rows;
-        const float *sr = src + b * s_src + r * ld_src;
-        float *dr = dst + b * s_dst + r * ld_dst;
+        const int64_t r = rb % j.rows, b = rb / j.rows;
+        const float *sr = j.src + b * j.s_src + r * j.ld_src;
+        float *dr = j.dst + b * j.s_dst + r * j.ld_dst;
+        // All eight loads go out before the first store (source and
+        // destination never overlap), so they are in flight together.
+        float v[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int64_t c = seg * 256 + q * 32 + lane;
-            if (c < cols) dr[c] = sr[c];
+            v[q] = c < j.cols ? __ldg(sr + c) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t c = seg * 256 + q * 32 + lane;
+            if (c < j.cols) dr[c] = v[q];
         }
     }
 }
 
 // dst[b * s_dst + c * ld_dst + r] = src[b * s_src + r * ld_src + c], through
-// 64 x 64 shared-memory tiles (padded by one column): 32 x 8 threads, each
-// moving 16 elements per tile, so reads (along c) and writes (along r) are
-// both 128-byte warp segments.
-__global__ void __launch_bounds__(256)
-pack_transpose_batched_kernel(const float *__restrict__ src, int64_t rows, int64_t cols,
-                              int64_t ld_src, int64_t s_src, float *__restrict__ dst,
-                              int64_t ld_dst, int64_t s_dst, int64_t batch)
+// 64 x 64 shared-memory tiles (padded by one column): 256 threads as 32 x 8,
+// each moving 16 elements per tile, so reads (along c) and writes (along r)
+// are both 128-byte warp segments.
+__device__ __forceinline__ void transpose_tiles(const PackJob &j, int64_t blk, int64_t nblk,
+                                                float (*tile)[65])
 {
-    __shared__ float tile[64][65];
-    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8 threads
-    const int64_t tiles_c = (cols + 63) / 64;
-    const int64_t per_entry = ((rows + 63) / 64) * tiles_c;
-    for (int64_t t = blockIdx.x; t < batch * per_entry; t += gridDim.x) {
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t tiles_c = (j.cols + 63) / 64;
+    const int64_t per_entry = ((j.rows + 63) / 64) * tiles_c;
+    for (int64_t t = blk; t < j.batch * per_entry; t += nblk) {
         const int64_t b = t / per_entry, tt = t % per_entry;
         const int64_t r0 = (tt / tiles_c) * 64, c0 = (tt % tiles_c) * 64;
-        const float *sb = src + b * s_src;
-        float *db = dst + b * s_dst;
+        const float *sb = j.src + b * j.s_src;
+        float *db = j.dst + b * j.s_dst;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int64_t r = r0 + ty + 8 * i;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int64_t c = c0 + tx + 32 * h;
-                tile[ty + 8 * i][tx + 32 * h] = (r < rows && c < cols) ? sb[r * ld_src + c] : 0.0f;
+                tile[ty + 8 * i][tx + 32 * h] = (r < j.rows && c < j.cols) ? __ldg(sb + r * j.ld_src + c) : 0.0f;
             }
         }
         __syncthreads();
@@ -185,10 +150,47 @@ pack_transpose_batched_kernel(const float *__restrict__ src, int64_t rows, int64
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int64_t r = r0 + tx + 32 * h;
-                if (c < cols && r < rows) db[c * ld_dst + r] = tile[tx + 32 * h][ty + 8 * i];
+                if (c < j.cols && r < j.rows) db[c * j.ld_dst + r] = tile[tx + 32 * h][ty + 8 * i];
             }
         }
         __syncthreads();
+    }
+}
+
+__device__ __forceinline__ void run_pack_job(const PackJob &j, int64_t blk, float (*tile)[65])
+{
+    if (j.transpose)
+        transpose_tiles(j, blk, j.blocks, tile);
+    else
+        copy_rows(j, blk, j.blocks);
+}
+
+__global__ void __launch_bounds__(256) pack_transpose_batched_kernel(const PackJob j)
+{
+    __shared__ float tile[64][65];
+    transpose_tiles(j, blockIdx.x, gridDim.x, tile);
+}
+
+// Both operands' layout passes of one product in one launch: blocks
+// [0, a.blocks) run job a, the next b.blocks run job b, and one more block
+// zeroes `zero_words` words (the product's stream-K arrival counters). Every
+// block first allows a kernel queued behind this one with programmatic
+// serialization (the product, which waits for this grid's completion before
+// it reads anything) to start taking SMs as this grid's last blocks run.
+// At most 40 registers a thread, so six blocks fit an SM (same-box A/B: a
+// hair faster than 48 registers and five on 4097 x 3001 x 2049).
+__global__ void __launch_bounds__(256, 6)
+pack_pair_kernel(const PackJob a, const PackJob b, unsigned int *zero, int64_t zero_words)
+{
+    __shared__ float tile[64][65];
+    ptx::grid_launch_dependents();
+    const int64_t blk = blockIdx.x;
+    if (blk < a.blocks) {
+        run_pack_job(a, blk, tile);
+    } else if (blk < a.blocks + b.blocks) {
+        run_pack_job(b, blk - a.blocks, tile);
+    } else {
+        for (int64_t w = threadIdx.x; w < zero_words; w += blockDim.x) zero[w] = 0u;
     }
 }
 
@@ -215,13 +217,13 @@ unsigned grid_for(int64_t work, int64_t per_block, int64_t cap)
 }
 }  // namespace
 
-cudaError_t launch_pack_batched(const float *src, int64_t rows, int64_t cols, int64_t ld_src,
-                                int64_t s_src, float *dst, int64_t ld_dst, int64_t s_dst,
-                                int64_t batch, cudaStream_t stream)
+PackJob pack_job(const float *src, int64_t rows, int64_t cols, int64_t ld_src, int64_t s_src, float *dst,
+                 int64_t ld_dst, int64_t s_dst, int64_t batch, bool transpose)
 {
-    pack_batched_kernel<<<grid_for(batch * rows * ((cols + 255) / 256), 8, 8192), 256, 0, stream>>>(
-        src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch);
-    return cudaGetLastError();
+    PackJob j{src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch, transpose ? 1 : 0, 0};
+    j.blocks = transpose ? grid_for(batch * ((rows + 63) / 64) * ((cols + 63) / 64), 1, 8192)
+                         : grid_for(batch * rows * ((cols + 255) / 256), 8, 8192);
+    return j;
 }
 
 cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_t cols,
@@ -229,9 +231,18 @@ cudaError_t launch_pack_transpose_batched(const float *src, int64_t rows, int64_
                                           int64_t ld_dst, int64_t s_dst, int64_t batch,
                                           cudaStream_t stream)
 {
-    const int64_t tiles = batch * ((rows + 63) / 64) * ((cols + 63) / 64);
-    pack_transpose_batched_kernel<<<grid_for(tiles, 1, 8192), dim3(32, 8), 0, stream>>>(
-        src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch);
+    const PackJob j = pack_job(src, rows, cols, ld_src, s_src, dst, ld_dst, s_dst, batch, true);
+    pack_transpose_batched_kernel<<<(unsigned)j.blocks, 256, 0, stream>>>(j);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_pair(const PackJob &a, const PackJob &b, unsigned int *zero, size_t zero_bytes,
+                             cudaStream_t stream)
+{
+    const int64_t zero_words = zero ? (int64_t)(zero_bytes / sizeof(unsigned int)) : 0;
+    const int64_t blocks = a.blocks + b.blocks + (zero_words > 0 ? 1 : 0);
+    if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    pack_pair_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a, b, zero, zero_words);
     return cudaGetLastError();
 }
 

@@ -34,6 +34,20 @@ size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
     }
 }
 
+size_t ffma_tma_counter_bytes(int kernel, const GemmArgs &g)
+{
+    switch (kernel) {
+    case kKernFfma128x128k32s4: return counter_bytes<CfgFfma128x128k32s4>(g);
+    case kKernFfma2_128x128k32s4: return counter_bytes<CfgFfma2_128x128k32s4>(g);
+    case kKernFfma2_128x128k16s8: return counter_bytes<CfgFfma2_128x128k16s8>(g);
+    case kKernFfma2_128x64k32s4: return counter_bytes<CfgFfma2_128x64k32s4>(g);
+    case kKernFfma2_128x256k32s4: return counter_bytes<CfgFfma2_128x256k32s4>(g);
+    case kKernFfma2_128x256k32s4ka: return counter_bytes<CfgFfma2_128x256k32s4ka>(g);
+    case kKernFfma2_128x128k32s4ka: return counter_bytes<CfgFfma2_128x128k32s4ka>(g);
+    default: return 0;
+    }
+}
+
 cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
 {
     // B arrives K x N (transposed ones packed); A arrives M x K, except for

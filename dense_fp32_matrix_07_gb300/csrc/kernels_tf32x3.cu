@@ -621,7 +621,7 @@ cudaError_t launch_cfg(const GemmArgs &g, cudaStream_t stream)
     if (sched.sk_ctas > 0 &&
         g.workspace_bytes < l.total + schedule_workspace_bytes(sched, kCounters, Cfg::BM * Cfg::CM, Cfg::BN))
         sched = tf32x3_schedule<Cfg>(g, false);
-    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, kCounters, stream)) != cudaSuccess)
+    if (sched.sk_ctas > 0 && (e = schedule_attach_workspace(sched, ws + l.total, kCounters, true, stream)) != cudaSuccess)
         return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0);
     float *C = g.C;

@@ -84,12 +84,18 @@ size_t schedule_workspace_bytes(const Schedule &s, int counters_per_tile, int bm
     return counter_bytes(s, counters_per_tile) + 2 * (size_t)s.sk_ctas * bm * bn * sizeof(float);
 }
 
-cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, cudaStream_t stream)
+size_t schedule_counter_bytes(const Schedule &s, int counters_per_tile)
+{
+    return s.sk_ctas == 0 ? 0 : counter_bytes(s, counters_per_tile);
+}
+
+cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, bool zero,
+                                      cudaStream_t stream)
 {
     const size_t cb = counter_bytes(s, counters_per_tile);
     s.counters = static_cast<unsigned *>(workspace);
     s.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cb);
-    return cudaMemsetAsync(s.counters, 0, cb, stream);
+    return zero ? cudaMemsetAsync(s.counters, 0, cb, stream) : cudaSuccess;
 }
 
 }  // namespace sgemm_gb300

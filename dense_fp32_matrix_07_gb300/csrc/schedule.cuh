@@ -173,8 +173,13 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int bm, int bn, int bk, 
 // bm x bn FP32 partial-sum slots per CTA of the stream-K region.
 size_t schedule_workspace_bytes(const Schedule &s, int counters_per_tile, int bm, int bn);
 
-// Points the schedule's counters and partial slots into `workspace` and
-// zeroes the counters on `stream`.
-cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, cudaStream_t stream);
+// Bytes of the arrival counters at the start of that workspace (0 without a
+// stream-K region).
+size_t schedule_counter_bytes(const Schedule &s, int counters_per_tile);
+
+// Points the schedule's counters and partial slots into `workspace` and, if
+// `zero`, zeroes the counters on `stream` (else the caller has).
+cudaError_t schedule_attach_workspace(Schedule &s, void *workspace, int counters_per_tile, bool zero,
+                                      cudaStream_t stream);
 
 }  // namespace sgemm_gb300

@@ -369,36 +369,39 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
             }
             return SGEMM_ERR_ALLOC;
         }
-        cudaError_t e = cudaSuccess;
-        if (pa) {
-            float *dst = reinterpret_cast<float *>(scratch);
-            const bool transpose = akm ? c.op_a == 0 : c.op_a == 1;
-            e = transpose ? launch_pack_transpose_batched(c.A, a_rows, a_cols, c.lda, c.sa, dst, lda_p,
-                                                          a_rows_p * lda_p, a_entries, stream)
-                          : launch_pack_batched(c.A, a_rows, a_cols, c.lda, c.sa, dst, lda_p, a_rows_p * lda_p,
-                                                a_entries, stream);
-            g.A = dst;
-            g.lda = lda_p;
-            g.stride_a = a_entries > 1 ? a_rows_p * lda_p : 0;
-        }
-        if (e == cudaSuccess && pb) {
-            float *dst = reinterpret_cast<float *>(scratch + a_bytes);
-            e = c.op_b == 1 ? launch_pack_transpose_batched(c.B, c.N, c.K, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p,
-                                                            b_entries, stream)
-                            : launch_pack_batched(c.B, c.K, c.N, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p, b_entries,
-                                                  stream);
-            g.B = dst;
-            g.ldb = ldb_p;
-            g.stride_b = b_entries > 1 ? c.K * ldb_p : 0;
-        }
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            cudaFreeAsync(scratch, stream);
-            return SGEMM_ERR_LAUNCH;
-        }
         if (ws_bytes > 0) {
             g.workspace = scratch + ws_off;
             g.workspace_bytes = ws_bytes;
+        }
+        if (pa || pb) {
+            // Both layout passes in one launch, which also zeroes the
+            // product's stream-K arrival counters; the product is queued
+            // right behind it and may start while its last blocks run.
+            PackJob ja{}, jb{};
+            if (pa) {
+                float *dst = reinterpret_cast<float *>(scratch);
+                const bool transpose = akm ? c.op_a == 0 : c.op_a == 1;
+                ja = pack_job(c.A, a_rows, a_cols, c.lda, c.sa, dst, lda_p, a_rows_p * lda_p, a_entries, transpose);
+                g.A = dst;
+                g.lda = lda_p;
+                g.stride_a = a_entries > 1 ? a_rows_p * lda_p : 0;
+            }
+            if (pb) {
+                float *dst = reinterpret_cast<float *>(scratch + a_bytes);
+                jb = c.op_b == 1 ? pack_job(c.B, c.N, c.K, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p, b_entries, true)
+                                 : pack_job(c.B, c.K, c.N, c.ldb, c.sb, dst, ldb_p, c.K * ldb_p, b_entries, false);
+                g.B = dst;
+                g.ldb = ldb_p;
+                g.stride_b = b_entries > 1 ? c.K * ldb_p : 0;
+            }
+            const size_t zero_bytes = config_counter_bytes(cfg, g);
+            if (launch_pack_pair(ja, jb, static_cast<unsigned int *>(g.workspace), zero_bytes, stream) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                cudaFreeAsync(scratch, stream);
+                return SGEMM_ERR_LAUNCH;
+            }
+            g.behind_pack = true;
         }
     }
 

@@ -35,10 +35,13 @@
  * memory pool on `stream` and returned on `stream`; it is never exposed.
  * Asynchrony: calls return after enqueueing work on `stream`; results are
  * ready when the stream's work completes. An FFMA call enqueues at most
- * four kernels (operand packing, the product, and the kernel of the last
- * rows that sgemm_plan_row_tail() describes) plus a memset of the stream-K
- * arrival counters; a 3xTF32 call enqueues two split passes and the
- * product per batch entry. No call synchronises the host.
+ * three kernels: one layout pass for the operands that need it (it also
+ * zeroes the stream-K arrival counters), the product, which may start while
+ * that pass finishes (programmatic dependent launch; its threads wait for
+ * the pass before they touch memory), and the kernel of the last rows that
+ * sgemm_plan_row_tail() describes. Without a layout pass, a memset of the
+ * arrival counters precedes the product. A 3xTF32 call enqueues two split
+ * passes and the product per batch entry. No call synchronises the host.
  * Graph capture: sgemm(), sgemm_ex(), sgemm_general() and sgemm_general_ex()
  * may be captured into a CUDA graph once one call has run on the device
  * (the first call sets the device up); a replay computes the product of
