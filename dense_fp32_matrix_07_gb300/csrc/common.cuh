@@ -41,9 +41,10 @@ struct GemmArgs {
     int op_a = 0, op_b = 0;
     // Set when this call's layout pass (launch_pack_pair) was queued right
     // before the product and has zeroed the stream-K arrival counters at the
-    // start of `workspace`: the product then skips its own zeroing and
-    // launches with programmatic stream serialization, its CTAs waiting for
-    // the pass to complete before they touch memory.
+    // start of `workspace`: the product then skips its own zeroing and, for K
+    // a multiple of the slab depth, launches with programmatic stream
+    // serialization, its threads waiting for the pass to complete before
+    // they touch global memory.
     bool behind_pack = false;
 };
 

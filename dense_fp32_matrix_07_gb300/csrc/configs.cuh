@@ -106,6 +106,12 @@ cudaError_t prepare_ffma_tma();
 // slab depth (kernels_ffma_tma_ktail.cu); launch_ffma_tma() dispatches there.
 cudaError_t launch_ffma_tma_ktail(int kernel, const GemmArgs &g, cudaStream_t stream);
 cudaError_t prepare_ffma_tma_ktail();
+// The same kernels (K a multiple of the slab depth) launched behind the
+// call's layout pass with programmatic serialization
+// (kernels_ffma_tma_dep.cu); launch_ffma_tma() dispatches there when
+// g.behind_pack is set.
+cudaError_t launch_ffma_tma_dep(int kernel, const GemmArgs &g, cudaStream_t stream);
+cudaError_t prepare_ffma_tma_dep();
 
 // Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
 cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);

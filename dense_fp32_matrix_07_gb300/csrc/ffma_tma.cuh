@@ -134,7 +134,9 @@ struct Epilogue {
     int a_bz, b_bz;
 };
 
-template <class Cfg, bool VEC_C, bool K_TAIL>
+// DEP: the instance launched behind the call's layout pass with
+// programmatic serialization (kernels_ffma_tma_dep.cu).
+template <class Cfg, bool VEC_C, bool K_TAIL, bool DEP = false>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapB,
@@ -170,8 +172,11 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
     __syncthreads();
     // Queued behind the call's layout pass with programmatic serialization,
     // this grid may start while that pass still runs: no thread touches
-    // global memory before the pass has completed (a no-op otherwise).
-    ptx::grid_dependency_wait();
+    // global memory before the pass has completed. Only the DEP instances
+    // carry the wait: in the others, where it would be a no-op, it still
+    // cost time (same-box A/B, 4096 x 3001 x 2048 with A stored transposed,
+    // no layout pass: 744.4 against 742.9 us).
+    if constexpr (DEP) ptx::grid_dependency_wait();
 
     if (warp >= Cfg::CONSUMERS) {
         // ------------------------------ producer ------------------------------
@@ -554,13 +559,13 @@ cudaError_t encode_3d(CUtensorMap *map, const float *ptr, int64_t rows, int64_t 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <class Cfg, bool K_TAIL>
+template <class Cfg, bool K_TAIL, bool DEP = false>
 cudaError_t set_smem_limit()
 {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_ffma_tma_kernel<Cfg, true, K_TAIL>,
+    cudaError_t e = cudaFuncSetAttribute(sgemm_ffma_tma_kernel<Cfg, true, K_TAIL, DEP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sgemm_ffma_tma_kernel<Cfg, false, K_TAIL>,
+    return cudaFuncSetAttribute(sgemm_ffma_tma_kernel<Cfg, false, K_TAIL, DEP>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
 }
 
@@ -589,8 +594,8 @@ size_t counter_bytes(const GemmArgs &g)
 }
 
 // Launches the product; K_TAIL selects the kernel that trims the last slab
-// (for K not a multiple of BK).
-template <class Cfg, bool K_TAIL>
+// (for K not a multiple of BK), DEP the launch behind the call's layout pass.
+template <class Cfg, bool K_TAIL, bool DEP = false>
 cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
 {
     CUtensorMap mapA, mapB;
@@ -619,12 +624,13 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     unsigned int *status = g.status;
     int withhold = g.withhold_it;
     void *args[] = {&mapA, &mapB, &ep, &s, &status, &withhold};
-    const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true, K_TAIL>)
-                         : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false, K_TAIL>);
+    const void *fn = vec ? reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, true, K_TAIL, DEP>)
+                         : reinterpret_cast<const void *>(sgemm_ffma_tma_kernel<Cfg, false, K_TAIL, DEP>);
     // No CTA waits for another (split tiles are reduced by their last part),
-    // so this is an ordinary launch; behind the call's layout pass it may
-    // start early (programmatic serialization), its CTAs waiting for the pass.
-    if (g.behind_pack) {
+    // so this is an ordinary launch; the DEP instance, behind the call's
+    // layout pass, may start early (programmatic serialization), its threads
+    // waiting for the pass.
+    if constexpr (DEP) {
         cudaLaunchConfig_t lc = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -17,7 +17,8 @@ cudaError_t prepare_ffma_tma()
     if ((e = set_smem_limit<CfgFfma2_128x256k32s4ka, false>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x128k32s4ka, false>()) != cudaSuccess) return e;
     if ((e = set_smem_limit<CfgFfma2_128x256k32s4, false>()) != cudaSuccess) return e;
-    return prepare_ffma_tma_ktail();
+    if ((e = prepare_ffma_tma_ktail()) != cudaSuccess) return e;
+    return prepare_ffma_tma_dep();
 }
 
 size_t ffma_tma_workspace_bytes(int kernel, const GemmArgs &g)
@@ -58,6 +59,9 @@ cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
     // slab (kernels_ffma_tma_ktail.cu); every configuration has BK 32 or 16.
     const int bk = kernel == kKernFfma2_128x128k16s8 ? 16 : 32;
     if (g.K % bk != 0) return launch_ffma_tma_ktail(kernel, g, stream);
+    // Behind the call's layout pass, the instances that may start while it
+    // finishes (kernels_ffma_tma_dep.cu).
+    if (g.behind_pack) return launch_ffma_tma_dep(kernel, g, stream);
     switch (kernel) {
     case kKernFfma128x128k32s4: return launch<CfgFfma128x128k32s4, false>(g, stream);
     case kKernFfma2_128x128k32s4: return launch<CfgFfma2_128x128k32s4, false>(g, stream);

@@ -376,7 +376,8 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
         if (pa || pb) {
             // Both layout passes in one launch, which also zeroes the
             // product's stream-K arrival counters; the product is queued
-            // right behind it and may start while its last blocks run.
+            // right behind it and (K a multiple of the slab depth) may
+            // start while its last blocks run.
             PackJob ja{}, jb{};
             if (pa) {
                 float *dst = reinterpret_cast<float *>(scratch);

@@ -36,9 +36,10 @@
  * Asynchrony: calls return after enqueueing work on `stream`; results are
  * ready when the stream's work completes. An FFMA call enqueues at most
  * three kernels: one layout pass for the operands that need it (it also
- * zeroes the stream-K arrival counters), the product, which may start while
- * that pass finishes (programmatic dependent launch; its threads wait for
- * the pass before they touch memory), and the kernel of the last rows that
+ * zeroes the stream-K arrival counters), the product, which for K a
+ * multiple of its slab depth may start while that pass finishes
+ * (programmatic dependent launch; its threads wait for the pass before they
+ * touch memory), and the kernel of the last rows that
  * sgemm_plan_row_tail() describes. Without a layout pass, a memset of the
  * arrival counters precedes the product. A 3xTF32 call enqueues two split
  * passes and the product per batch entry. No call synchronises the host.
