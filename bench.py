@@ -80,8 +80,8 @@ PROFILE_RECORD = os.path.join(ROOT, "profiles", "ffma_tma_sq4096.json")
 TENSOR_CONFIG = "tf32x3_pair_128x256_k16_s4"
 TENSOR_FALLBACK_CONFIG = "tf32x3_128x256_k16_s4"
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_fp32_matrix_07_gb300", "csrc", f)
-                  for f in ("ffma_tma.cuh", "kernels_ffma_tma.cu", "kernels_ffma_tma_ktail.cu", "ptx.cuh",
-                            "schedule.cuh", "schedule.cu")]
+                  for f in ("ffma_tma.cuh", "kernels_ffma_tma.cu", "kernels_ffma_tma_ktail.cu",
+                            "kernels_ffma_tma_dep.cu", "ptx.cuh", "schedule.cuh", "schedule.cu")]
 
 
 def product_flops(M: int, N: int, K: int) -> float:
