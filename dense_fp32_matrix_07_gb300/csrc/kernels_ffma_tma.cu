@@ -56,9 +56,17 @@ cudaError_t launch_ffma_tma(int kernel, const GemmArgs &g, cudaStream_t stream)
     const int want_op_a = (kernel == kKernFfma2_128x256k32s4ka || kernel == kKernFfma2_128x128k32s4ka) ? 1 : 0;
     if (g.op_a != want_op_a || g.op_b != 0) return cudaErrorInvalidValue;
     // A K that is not a multiple of BK runs the kernels that trim the last
-    // slab (kernels_ffma_tma_ktail.cu); every configuration has BK 32 or 16.
+    // slab (kernels_ffma_tma_ktail.cu) when that slab holds at most 3/8 of
+    // BK valid k; every configuration has BK 32 or 16. The trimmed slab is
+    // multiplied one k at a time, so past that point the whole zero-filled
+    // slab of the main loop is the faster one (same-box sweep, trimmed
+    // against whole, k_last 4 / 12 / 20 of 32: 4096 x 4096 x 2048+k_last
+    // 1009.6 / 1013.7 / 1017.2 against 1013.2 us, 4096 x 3001 x 2048+k_last
+    // 777.3 / 780.3 / 783.5 against 780.5 us, 4096 x 1536 x 1024+k_last on
+    // the row-major 128 x 256 tiles 216.6 / 216.9 / 218.6 against 218.6 us).
     const int bk = kernel == kKernFfma2_128x128k16s8 ? 16 : 32;
-    if (g.K % bk != 0) return launch_ffma_tma_ktail(kernel, g, stream);
+    const int k_last = (int)(g.K % bk);
+    if (k_last != 0 && 8 * k_last <= 3 * bk) return launch_ffma_tma_ktail(kernel, g, stream);
     // Behind the call's layout pass, the instances that may start while it
     // finishes (kernels_ffma_tma_dep.cu).
     if (g.behind_pack) return launch_ffma_tma_dep(kernel, g, stream);

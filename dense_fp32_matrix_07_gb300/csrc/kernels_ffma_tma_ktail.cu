@@ -1,8 +1,9 @@
 // Instantiations of the main SGEMM kernel (ffma_tma.cuh) that trim the last
 // K slab: for a K that is not a multiple of the slab depth, the last slab of
 // every tile multiplies only its k_last valid k instead of a whole slab of
-// zero-filled padding. A separate translation unit, so these kernels compile
-// in parallel with the others.
+// zero-filled padding. launch_ffma_tma() takes them when k_last is at most
+// 3/8 of the slab depth. A separate translation unit, so these kernels
+// compile in parallel with the others.
 #include "ffma_tma.cuh"
 
 namespace sgemm_gb300 {

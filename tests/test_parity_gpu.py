@@ -48,6 +48,25 @@ def test_shape_sweep_float(cuda_device, oracle, config):
         check_untouched_padding(dC, N)
 
 
+FFMA_TMA = [i for i in CONFIGS if sg.sgemm_config_name(i).startswith("ffma")]
+
+
+@pytest.mark.parametrize("config", FFMA_TMA, ids=[sg.sgemm_config_name(i) for i in FFMA_TMA])
+def test_k_tail_both_kernels(cuda_device, oracle, config):
+    """K = 64 + k_last on both sides of the point where the call stops
+    trimming the last slab (k_last <= 3/8 of the slab depth: 12 of 32, 6 of
+    16) and multiplies the whole zero-filled slab instead; integer inputs,
+    so both kernels must match the oracle exactly, on a stream-K schedule
+    (M, N give several tiles) and with a ragged last row block."""
+    for n, k_last in enumerate((1, 6, 7, 12, 13, 31)):
+        M, N, K = 300, 260, 64 + k_last
+        A, B = workloads.make_operands(M, N, K, "int", 700 + n)
+        rc, C, dC = run(M, N, K, A, K, B, N, config=config)
+        assert rc == 0, (K, sg.sgemm_error_string(rc))
+        _oracle_check(oracle, M, N, K, A, K, B, N, C, True, f"cfg {config} K={K}")
+        check_untouched_padding(dC, N)
+
+
 @pytest.mark.parametrize("config", CONFIGS, ids=CFG_IDS)
 def test_shape_sweep_integer_exact(cuda_device, oracle, config):
     for n, (M, N, K) in enumerate(_shapes(2000 + config, 25)):
