@@ -561,7 +561,9 @@ def main():
                     help="time an ad-hoc MxNxK product (tight strides, N(0,1) inputs, seed 0) "
                          "instead of a named workload")
     ap.add_argument("--config", type=int, default=-1, help="force a kernel config id")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of each e2e leg (default: the timed steps up to 30, or about 0.25 s of "
+                         "device time if that is more, so the first copy in and the last copy out weigh little)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-copy legs")
     ap.add_argument("--no-tf32x3", action="store_true",
@@ -739,7 +741,13 @@ def run_ours(args, local, extra):
     # on one stream; "pipelined" is how a caller streams independent steps:
     # two buffer sets and three streams, so the copies of one step overlap
     # the product of another.
-    e2e_steps = max(2, min(args.e2e_steps, args.steps))
+    # Each leg starts with a copy in and ends with a copy out that overlap no
+    # product (about 1 ms at 4096^3): spread over the timed steps (at most
+    # 30), or over about a quarter second of device time if that is more.
+    if args.e2e_steps is not None:
+        e2e_steps = max(2, args.e2e_steps)
+    else:
+        e2e_steps = max(2, min(args.steps, 30), int(0.25 / max(statistics.median(kernel_ms) / 1e3, 1e-6)))
     if not args.no_e2e:
         hA = A.pin_memory()
         hB = B.pin_memory()
