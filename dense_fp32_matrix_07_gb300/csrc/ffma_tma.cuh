@@ -167,16 +167,21 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap mapA,
         // A kernel queued behind this one with programmatic serialization
         // (the last-rows kernel, which reads nothing this grid writes) may
         // take SMs as soon as this persistent grid's CTAs leave them.
-        ptx::grid_launch_dependents();
+        if constexpr (!DEP) ptx::grid_launch_dependents();
     }
     __syncthreads();
-    // Queued behind the call's layout pass with programmatic serialization,
-    // this grid may start while that pass still runs: no thread touches
-    // global memory before the pass has completed. Only the DEP instances
-    // carry the wait: in the others, where it would be a no-op, it still
-    // cost time (same-box A/B, 4096 x 3001 x 2048 with A stored transposed,
-    // no layout pass: 744.4 against 742.9 us).
-    if constexpr (DEP) ptx::grid_dependency_wait();
+    if constexpr (DEP) {
+        // Queued behind the call's layout pass with programmatic
+        // serialization, this grid may start while that pass still runs: no
+        // thread touches global memory before the pass has completed. Only
+        // the DEP instances carry the wait: in the others, where it would be
+        // a no-op, it still cost time (same-box A/B, 4096 x 3001 x 2048 with A
+        // stored transposed, no layout pass: 744.4 against 742.9 us). The
+        // last-rows kernel behind this grid reads the pass's copy of B, so it
+        // is let in only once the pass is complete.
+        ptx::grid_dependency_wait();
+        if (threadIdx.x == 0) ptx::grid_launch_dependents();
+    }
 
     if (warp >= Cfg::CONSUMERS) {
         // ------------------------------ producer ------------------------------

@@ -111,3 +111,25 @@ def test_row_tail_with_k_split_across_a_cluster(cuda_device, oracle, M, N, K):
         Cref, S = oracle.sgemm(M, N, K, A.numpy(), K, B.numpy(), N)
         assert_parity(C, Cref, S, exact, f"{M}x{N}x{K} {dist}")
         check_untouched_padding(dC, N)
+
+
+def test_row_tail_behind_layout_pass_with_idle_sms(cuda_device, oracle):
+    # The tail kernel reads the copy of B that the call's layout pass writes.
+    # Here B's rows are not 16-byte aligned (ldb = 2051), so the pass copies
+    # B, and the forced whole-tile 128x256 configuration runs only 8 product
+    # CTAs: most SMs stay free for the tail kernel the moment the product
+    # lets it in. It must not read B's copy before the pass has completed.
+    # Each repetition draws a new B, so a stale copy from the repetition
+    # before (the pool hands back the same scratch) would show in row 128.
+    cfg = sg.config_ids()["ffma2_128x256_k32_s4_dp"]
+    M, N, K, ldb = 129, 2048, 1024, 2051
+    rc, _, pa, pb = sg.sgemm_general_plan(0, 0, M, N, K, 1.0, K, 0, ldb, 0, 0.0, N, 0, 1, 0, 0, 0,
+                                          torch.cuda.get_device_properties(0).multi_processor_count, cfg)
+    assert rc == 0 and (pa, pb) == (0, 1) and _tail_rows(cfg, M, N, K) == 1
+    for rep in range(20):
+        A, B = workloads.make_operands(M, N, K, "int", 300 + rep, ldb=ldb)
+        rc, C, dC = run(M, N, K, A, K, B, ldb, config=cfg)
+        assert rc == 0
+        Cref, S = oracle.sgemm(M, N, K, A.numpy(), K, B.numpy(), ldb)
+        assert_parity(C, Cref, S, True, f"rep {rep}")
+        check_untouched_padding(dC, N)
