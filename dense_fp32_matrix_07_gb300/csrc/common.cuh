@@ -46,6 +46,9 @@ struct GemmArgs {
     // serialization, its threads waiting for the pass to complete before
     // they touch global memory.
     bool behind_pack = false;
+    // Set when the caller has zeroed the stream-K arrival counters at the
+    // start of `workspace` (the layout pass or one memset of the call).
+    bool counters_zeroed = false;
 };
 
 // Bits of the device error word.

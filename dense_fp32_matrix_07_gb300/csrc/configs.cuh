@@ -131,8 +131,18 @@ struct RowTailArgs {
     int r;               // rows, 1 .. kRowTailMax
     int64_t N, K, batch;
     float alpha, beta;
+    // With more than one K chunk per column block (row_tail_splits() > 1):
+    // the arrival counters (zero at launch, row_tail_counter_bytes()) and the
+    // chunk sums (row_tail_slot_bytes()).
+    unsigned int *counters;
+    float *slots;
 };
 cudaError_t launch_row_tail(const RowTailArgs &t, int num_sms, cudaStream_t stream);
+// K chunks per column block of the row-tail kernel, and the bytes of its
+// counters (a multiple of 256) and chunk sums; both 0 with one chunk.
+int row_tail_splits(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms);
+size_t row_tail_counter_bytes(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms);
+size_t row_tail_slot_bytes(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms);
 
 // Rows that a call with this configuration leaves to the row-tail kernel:
 // M = 128 q + r with 1 <= r <= kRowTailMax on a TMA FFMA configuration, when

@@ -621,7 +621,7 @@ cudaError_t launch(const GemmArgs &g, cudaStream_t stream)
     Schedule s = make_schedule<Cfg>(g, g.workspace != nullptr);
     if (s.sk_ctas > 0 && g.workspace_bytes < workspace_bytes<Cfg>(s)) s = make_schedule<Cfg>(g, false);
     if (s.sk_ctas > 0 &&
-        (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, !g.behind_pack, stream)) != cudaSuccess)
+        (e = schedule_attach_workspace(s, g.workspace, Cfg::CONSUMERS, !g.counters_zeroed, stream)) != cudaSuccess)
         return e;
     const bool vec = ((reinterpret_cast<uintptr_t>(g.C) & 15u) == 0) && (g.ldc % 4 == 0) &&
                      (g.batch <= 1 || g.stride_c % 4 == 0);

@@ -3,29 +3,30 @@
 // The TMA kernels cover C with 128-row block rows, so an M just past a
 // multiple of 128 (4097 = 32 * 128 + 1) pads a whole block row of tiles
 // for a handful of real rows: 3 % of the FMAs at 4097 x 3001 x 2049. The
-// library then runs the tiled product on the first M - r rows only and this
+// library then runs the tiled product on the first M - r rows and this
 // kernel on the last r <= 8: each row is the course page's dot product of a
 // row of A with every column of B ("Перемножение матриц: наивное и
 // тайловое", section 1), here r rows at a time against one streamed pass
 // over B.
 //
 // Layout of the work: a CTA owns 128 columns (a float4 of B per lane) and a
-// contiguous chunk of K; its 8 warps split that chunk again. Clusters of ks
-// CTAs (ks <= 8) span all of K for the same columns. Each CTA adds its 8
-// warps' sums in warp order in shared memory; after a cluster barrier, rank
-// 0 reads the other CTAs' sums through distributed shared memory and adds
-// them in rank order, so the result is deterministic (integer-valued inputs
-// stay exact) and no global scratch, counter or memset is needed. A second
-// cluster barrier keeps every CTA's shared memory alive until rank 0 is done.
+// contiguous chunk of K (one of ks, its blockIdx.y); its 8 warps split that
+// chunk again. Each CTA adds its 8 warps' sums in warp order in shared
+// memory. With ks > 1 it writes that sum to a slot of its own and counts
+// itself in its column block's arrival counter; the CTA that completes the
+// count adds the ks slots in chunk order and stores C, so the result is
+// deterministic (integer-valued inputs stay exact) and no CTA waits for
+// another. The CTAs need no cluster, so each can start on the first SM the
+// product leaves.
 //
 // The kernel runs right after the tiled product, which reads and writes
 // nothing of its rows: it is launched with programmatic stream
 // serialization, so its CTAs take SMs as the product's persistent CTAs
-// finish (the product signals its dependents at its start), and it waits
-// for the product's completion only at its very end.
+// finish, and it waits for the product's completion only at its very end.
 #include "common.cuh"
 #include "configs.cuh"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace sgemm_gb300 {
 
@@ -43,13 +44,12 @@ __global__ void __launch_bounds__(kTailThreads)
 row_tail_kernel(const RowTailArgs t)
 {
     __shared__ float4 part[kTailWarps][R][32];
-    __shared__ float4 cta_sum[R][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t rank = ptx::cluster_ctarank(), ks = ptx::cluster_nctarank();
-    const int64_t b = blockIdx.z;
-    const int64_t col = (int64_t)blockIdx.x * kTailCols + 4 * lane;
-    // This CTA's chunk of K (its cluster rank), then this warp's share.
-    const int64_t c0 = t.K * rank / ks, c1 = t.K * (rank + 1) / ks;
+    const int ks = (int)gridDim.y, chunk = (int)blockIdx.y;
+    const int64_t b = blockIdx.z, cb = blockIdx.x;
+    const int64_t col = cb * kTailCols + 4 * lane;
+    // This CTA's chunk of K, then this warp's share.
+    const int64_t c0 = t.K * chunk / ks, c1 = t.K * (chunk + 1) / ks;
     const int64_t k0 = c0 + (c1 - c0) * w / kTailWarps, k1 = c0 + (c1 - c0) * (w + 1) / kTailWarps;
     const float *Ab = t.A + b * t.stride_a + t.m0 * t.a_row_stride;
     const float *Bb = t.B + b * t.stride_b;
@@ -103,45 +103,60 @@ row_tail_kernel(const RowTailArgs t)
     for (int i = 0; i < R; ++i) part[w][i][lane] = acc[i];
     __syncthreads();
     if (w == 0) {
+        float4 s[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            float4 s = part[0][i][lane];
+            s[i] = part[0][i][lane];
             for (int v = 1; v < kTailWarps; ++v) {
                 const float4 p = part[v][i][lane];
-                s.x += p.x;
-                s.y += p.y;
-                s.z += p.z;
-                s.w += p.w;
+                s[i].x += p.x;
+                s[i].y += p.y;
+                s[i].z += p.z;
+                s[i].w += p.w;
             }
-            cta_sum[i][lane] = s;
         }
-    }
-    // Every CTA's sums are in its shared memory.
-    ptx::cluster_sync_all();
-    if (rank == 0 && w == 0 && col < t.N) {
-        const uint32_t base = ptx::smem_addr(&cta_sum[0][0]);
+        bool store = ks == 1;
+        if (!store) {
+            // Publish this chunk's sum, then count it; the chunk that
+            // completes the count adds all ks sums in chunk order.
+            const int64_t blk = b * gridDim.x + cb;
+            float4 *slots = reinterpret_cast<float4 *>(t.slots) + blk * (ks * R * 32);
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-            float4 s = cta_sum[i][lane];
-            for (uint32_t q = 1; q < ks; ++q) {
-                const float4 p = ptx::ld_shared_cluster_f4(base + (uint32_t)(i * 32 + lane) * 16u, q);
-                s.x += p.x;
-                s.y += p.y;
-                s.z += p.z;
-                s.w += p.w;
-            }
-            float *crow = t.C + b * t.stride_c + (t.m0 + i) * t.ldc + col;
-            const float v[4] = {s.x, s.y, s.z, s.w};
+            for (int i = 0; i < R; ++i) slots[(chunk * R + i) * 32 + lane] = s[i];
+            __threadfence();
+            __syncwarp();
+            unsigned before = 0;
+            if (lane == 0) before = atomic_inc_acq_rel_gpu(t.counters + blk);
+            store = __shfl_sync(0xffffffffu, before, 0) == (unsigned)(ks - 1);
+            if (store) {
+                (void)ld_acquire_gpu(t.counters + blk);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (col + e < t.N) {
-                    const float y = t.alpha * v[e];
-                    crow[e] = t.beta != 0.0f ? fmaf(t.beta, crow[e], y) : y;
+                for (int i = 0; i < R; ++i) {
+                    s[i] = slots[i * 32 + lane];
+                    for (int q = 1; q < ks; ++q) {
+                        const float4 p = slots[(q * R + i) * 32 + lane];
+                        s[i].x += p.x;
+                        s[i].y += p.y;
+                        s[i].z += p.z;
+                        s[i].w += p.w;
+                    }
                 }
+            }
+        }
+        if (store && col < t.N) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                float *crow = t.C + b * t.stride_c + (t.m0 + i) * t.ldc + col;
+                const float v[4] = {s[i].x, s[i].y, s[i].z, s[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < t.N) {
+                        const float y = t.alpha * v[e];
+                        crow[e] = t.beta != 0.0f ? fmaf(t.beta, crow[e], y) : y;
+                    }
+            }
         }
     }
-    // No CTA leaves (releasing its shared memory) before rank 0 has read it.
-    ptx::cluster_sync_all();
     // Launched behind the tiled product with programmatic serialization,
     // this grid may run while that one finishes; it does not complete before
     // that grid has, so whatever the stream runs next sees both.
@@ -155,34 +170,56 @@ constexpr RowTailKernel kRowTailKernels[kRowTailMax] = {
 
 }  // namespace
 
+int row_tail_splits(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms)
+{
+    // Enough CTAs to cover the SMs about three times over, at least 4 k per
+    // warp, at most 16 chunks for one row and 8 for more (the chunk sums
+    // the last CTA adds grow with the rows; same-box A/B of 16 against 8:
+    // 4097 x 3001 x 2049 778.4 against 779.4 us, 1025 x 1024 x 2048 81.3
+    // against 83.0 us, but 4100 x 3001 x 2049 787.5 against 783.4 us).
+    const int max_splits = r == 1 ? 16 : 8;
+    const int64_t col_blocks = (N + kTailCols - 1) / kTailCols;
+    int ks = 1;
+    while (ks < max_splits && col_blocks * ks * 2 * batch <= 3 * (int64_t)num_sms &&
+           K >= (int64_t)ks * 2 * kTailWarps * 4)
+        ks *= 2;
+    return ks;
+}
+
+size_t row_tail_counter_bytes(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms)
+{
+    if (row_tail_splits(r, N, K, batch, num_sms) == 1) return 0;
+    const size_t n = (size_t)((N + kTailCols - 1) / kTailCols) * (size_t)batch * sizeof(unsigned);
+    return (n + 255) / 256 * 256;
+}
+
+size_t row_tail_slot_bytes(int64_t r, int64_t N, int64_t K, int64_t batch, int num_sms)
+{
+    const int ks = row_tail_splits(r, N, K, batch, num_sms);
+    if (ks == 1) return 0;
+    return (size_t)((N + kTailCols - 1) / kTailCols) * (size_t)batch * ks * r * kTailCols * sizeof(float);
+}
+
 cudaError_t launch_row_tail(const RowTailArgs &t, int num_sms, cudaStream_t stream)
 {
     if (t.r < 1 || t.r > kRowTailMax || t.N < 1 || t.K < 1 || t.batch < 1 || t.batch > 65535)
         return cudaErrorInvalidValue;
     const int64_t col_blocks = (t.N + kTailCols - 1) / kTailCols;
     if (col_blocks > 0x7fffffff) return cudaErrorInvalidValue;
-    // Clusters of ks CTAs split K: enough CTAs to cover the SMs about once
-    // and a half, at least 4 k per warp.
-    int ks = 1;
-    while (ks < 8 && col_blocks * ks * t.batch * 2 < 3 * (int64_t)num_sms &&
-           t.K >= (int64_t)ks * 2 * kTailWarps * 4)
-        ks *= 2;
+    const int ks = row_tail_splits(t.r, t.N, t.K, t.batch, num_sms);
+    if (ks > 1 && (t.counters == nullptr || t.slots == nullptr)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t lc = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)ks;
-    attr[0].val.clusterDim.z = 1;
-    // It may start on SMs that the tiled product (which signals its
-    // dependents at its start) leaves before the whole grid has finished.
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    // It may start on SMs that the tiled product leaves before the whole
+    // grid has finished.
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.gridDim = dim3((unsigned)col_blocks, (unsigned)ks, (unsigned)t.batch);
     lc.blockDim = dim3(kTailThreads);
     lc.dynamicSmemBytes = 0;
     lc.stream = stream;
     lc.attrs = attr;
-    lc.numAttrs = 2;
+    lc.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&lc, kRowTailKernels[t.r - 1], t);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

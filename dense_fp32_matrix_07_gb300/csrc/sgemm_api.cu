@@ -353,7 +353,15 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
     if (pa) g.op_a = akm ? 1 : 0;
     if (pb) g.op_b = 0;
     const size_t ws_bytes = config_workspace_bytes(cfg, g);
-    const size_t total = ws_off + ws_bytes;
+    // Scratch: [packed A | packed B | the row-tail kernel's arrival counters |
+    // the product's stream-K workspace (its counters first) | the row-tail
+    // kernel's chunk sums]. Both kinds of counter are one contiguous range,
+    // zeroed once before the product.
+    const size_t tail_cnt_bytes = tail > 0 ? row_tail_counter_bytes(tail, c.N, c.K, c.batch, dev->num_sms) : 0;
+    const size_t tail_slot_bytes = tail > 0 ? row_tail_slot_bytes(tail, c.N, c.K, c.batch, dev->num_sms) : 0;
+    const size_t sk_off = ws_off + tail_cnt_bytes;
+    const size_t slot_off = sk_off + (ws_bytes + 255) / 256 * 256;
+    const size_t total = (ws_bytes + tail_cnt_bytes + tail_slot_bytes) > 0 ? slot_off + tail_slot_bytes : ws_off;
     uint8_t *scratch = nullptr;
     if (total > 0) {
         if (take_test_alloc_failure() ||
@@ -370,9 +378,13 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
             return SGEMM_ERR_ALLOC;
         }
         if (ws_bytes > 0) {
-            g.workspace = scratch + ws_off;
+            g.workspace = scratch + sk_off;
             g.workspace_bytes = ws_bytes;
         }
+        // The counters to zero before the product: the tail kernel's, then the
+        // stream-K ones at the start of the product's workspace.
+        const size_t zero_bytes = tail_cnt_bytes + config_counter_bytes(cfg, g);
+        unsigned int *const zero = reinterpret_cast<unsigned int *>(scratch + ws_off);
         if (pa || pb) {
             // Both layout passes in one launch, which also zeroes the
             // product's stream-K arrival counters; the product is queued
@@ -395,14 +407,20 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
                 g.ldb = ldb_p;
                 g.stride_b = b_entries > 1 ? c.K * ldb_p : 0;
             }
-            const size_t zero_bytes = config_counter_bytes(cfg, g);
-            if (launch_pack_pair(ja, jb, static_cast<unsigned int *>(g.workspace), zero_bytes, stream) !=
-                cudaSuccess) {
+            if (launch_pack_pair(ja, jb, zero_bytes > 0 ? zero : nullptr, zero_bytes, stream) != cudaSuccess) {
                 cudaGetLastError();
                 cudaFreeAsync(scratch, stream);
                 return SGEMM_ERR_LAUNCH;
             }
             g.behind_pack = true;
+            g.counters_zeroed = true;
+        } else if (tail_cnt_bytes > 0) {
+            if (cudaMemsetAsync(zero, 0, zero_bytes, stream) != cudaSuccess) {
+                cudaGetLastError();
+                cudaFreeAsync(scratch, stream);
+                return SGEMM_ERR_LAUNCH;
+            }
+            g.counters_zeroed = true;
         }
     }
 
@@ -427,6 +445,8 @@ static int sgemm_call(const Call &c, cudaStream_t stream)
         t.batch = c.batch;
         t.alpha = c.alpha;
         t.beta = c.beta;
+        t.counters = tail_cnt_bytes > 0 ? reinterpret_cast<unsigned int *>(scratch + ws_off) : nullptr;
+        t.slots = tail_slot_bytes > 0 ? reinterpret_cast<float *>(scratch + slot_off) : nullptr;
         err = launch_row_tail(t, dev->num_sms, stream);
     }
     if (scratch) cudaFreeAsync(scratch, stream);

@@ -266,8 +266,8 @@ int sgemm_plan(int64_t M, int64_t N, int64_t K,
  * product on the first M - r rows and a small kernel on the last r: each of
  * those rows is the dot product of a row of A with every column of B, as
  * the course page "Перемножение матриц: наивное и тайловое", section 1,
- * defines C, computed by clusters of CTAs that split K and add their parts
- * in a fixed order. Arguments: `config`, the configuration the call runs
+ * defines C, computed by CTAs that split K, the last of each column block
+ * adding the parts in a fixed order. Arguments: `config`, the configuration the call runs
  * (from sgemm_plan() or sgemm_general_plan(), or a forced one); M, N, K and
  * `batch` of the call. *out_rows receives r, or 0 when the call has no such
  * kernel (which adds one launch when it runs). Returns SGEMM_OK, or

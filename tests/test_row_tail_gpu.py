@@ -1,6 +1,7 @@
 """GPU parity of the row-tail path: for M = 128 q + r (1 <= r <= 8) the TMA
 configurations run the tiled product on the first M - r rows and a
-cluster kernel on the last r rows. Every case is checked against the FP64
+kernel on the last r rows (CTAs that split K, the last of each column
+block adding the parts in order). Every case is checked against the FP64
 oracle over all of C (float inputs within 1e-4 * sum|A_ik B_kj|, integer
 inputs bit-exact), with the planner confirming that the tail kernel runs."""
 
@@ -98,9 +99,9 @@ def test_row_tail_in_the_general_form(cuda_device, oracle, op_a, op_b, alpha, be
 
 
 @pytest.mark.parametrize("M,N,K", [(131, 300, 8000), (4097, 1024, 20000), (261, 2000, 12345)])
-def test_row_tail_with_k_split_across_a_cluster(cuda_device, oracle, M, N, K):
-    # Few column blocks, or a long K: clusters of 8 CTAs split K and rank 0
-    # adds their sums through distributed shared memory.
+def test_row_tail_with_k_split_across_ctas(cuda_device, oracle, M, N, K):
+    # Few column blocks, or a long K: up to 16 CTAs per column block split K
+    # and the last to finish adds their sums in chunk order.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rc, cfg, _, _ = sg.sgemm_plan(M, N, K, K, N, N, 0, 0, 0, sms)
     assert rc == 0 and _tail_rows(cfg, M, N, K) == M % 128
