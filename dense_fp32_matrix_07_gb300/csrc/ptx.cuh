@@ -182,21 +182,6 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 16 bytes at shared-memory offset `addr` of the cluster's CTA `rank`
-// (distributed shared memory; the peer must keep that memory alive, e.g. by
-// a cluster barrier after the read).
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr, uint32_t rank)
-{
-    float4 v;
-    asm volatile("{\n\t.reg .b32 ra;\n\t"
-                 "mapa.shared::cluster.u32 ra, %4, %5;\n\t"
-                 "ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [ra];\n\t}"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr), "r"(rank)
-                 : "memory");
-    return v;
-}
-
 // One arrival on the mbarrier at offset `bar` of the cluster's CTA `rank`.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank)
 {
