@@ -137,6 +137,22 @@ def profiled_traffic(config_name: str):
     return float(val)
 
 
+def call_launches(sg, cfg, M, N, K, lda, ldb, ldc, a, b, c, num_sms, config=-1, op_a=0, op_b=0,
+                  alpha=1.0, beta=0.0, sa=0, sb=0, sc=0, batch=1):
+    """(kernels of the library one sgemm_general_ex() call launches, as the
+    library itself plans them; what runs beside the product, in words)."""
+    rc, n = sg.sgemm_general_plan_launches(op_a, op_b, M, N, K, alpha, lda, sa, ldb, sb, beta, ldc, sc, batch,
+                                           a, b, c, num_sms, config)
+    if rc != 0:
+        raise RuntimeError(f"plan: {sg.sgemm_error_string(rc)}")
+    if not sg.sgemm_config_name(cfg).startswith("ffma"):
+        return n, ([f"{2 * batch} 3xTF32 split passes ({batch} entries, one product launch each)"]
+                   if sg.sgemm_config_name(cfg).startswith("tf32") else [])
+    tail = sg.sgemm_plan_row_tail(cfg, M, N, K, batch)[1] > 0
+    other = ["the layout pass (operand copies, counter zeroing)"] if n - 1 - tail > 0 else []
+    return n, other + (["the last-rows kernel"] if tail else [])
+
+
 def measured_tf32_tflops() -> tuple:
     """(TF32 dense tensor peak in TFLOP/s, basis): the measured BF16 burst
     peak scaled by the nominal TF32/BF16 ratio 1.1/2.25, else the profiling
@@ -517,6 +533,7 @@ def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_i
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     _, cfg, pa, pb = sg.sgemm_plan(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, dA.data_ptr(), dB.data_ptr(),
                                    dC.data_ptr(), num_sms)
+    a_addr, b_addr, c_addr = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
     total = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
     flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev) if total <= L2_BYTES else None
 
@@ -541,7 +558,8 @@ def measure_extra_workload(sg, w, dev, stream, steps, warmup, peak_tflops, gpu_i
             "fp32_peak_pct": round(100.0 * value / 1e3 / peak_tflops, 2),
             "best_step_fp32_peak_pct": round(100.0 * best / 1e3 / peak_tflops, 2),
             "steps": len(ms),
-            "launches_per_step": 1 + (1 if pa or pb else 0) + (1 if sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1] > 0 else 0),
+            "launches_per_step": call_launches(sg, cfg, w.M, w.N, w.K, w.lda, w.ldb, w.ldc, a_addr, b_addr,
+                                               c_addr, num_sms)[0],
             "step_ms": {"median": round(statistics.median(ms), 4), "best": round(min(ms), 4),
                         "mean": round(statistics.mean(ms), 4)},
             "l2": l2,
@@ -645,15 +663,16 @@ def run_ours(args, local, extra):
             if w.K * r32(w.M) + (w.K * r32(w.N) if pb else 0) > (16 << 20):
                 cfg = sg.config_ids()[sg.sgemm_config_name(cfg)[:-3]]
                 pa = int(dA.data_ptr() % 16 != 0 or w.lda % 4 != 0)
-        # The operand layout pass (one launch for both operands; sgemm_noalloc
-        # launches one per operand), the product and, for an M just past a
-        # multiple of the block height, the kernel of the last rows
-        # (sgemm_noalloc has none).
-        tail = 0 if args.noalloc else sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K)[1]
-        packs = pa + pb if args.noalloc else (1 if pa or pb else 0)
-        launches_per_step = 1 + packs + (1 if tail > 0 else 0)
-        other_launches = ([f"{packs} operand layout pass(es)"] if packs else []) + \
-            (["the last-rows kernel"] if tail > 0 else [])
+        # sgemm_noalloc launches one pass per packed operand and the product
+        # (its stream-K counters are zeroed by a memset); sgemm_ex() what the
+        # library plans for the call.
+        if args.noalloc:
+            launches_per_step = 1 + pa + pb
+            other_launches = [f"{pa + pb} operand layout pass(es)"] if pa + pb else []
+        else:
+            launches_per_step, other_launches = call_launches(sg, cfg, w.M, w.N, w.K, w.lda, w.ldb, w.ldc,
+                                                              dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                                              num_sms, args.config)
         total_bytes = 4 * (w.M * w.lda + w.K * w.ldb + w.M * w.ldc)
         flops = product_flops(w.M, w.N, w.K)
 
@@ -683,12 +702,9 @@ def run_ours(args, local, extra):
                                                 dB.data_ptr(), dC.data_ptr(), num_sms, args.config)
         if rc != 0:
             raise SystemExit(f"general form: {sg.sgemm_error_string(rc)}")
-        packs = sg.sgemm_config_name(cfg).startswith("ffma")
-        tail = sg.sgemm_plan_row_tail(cfg, w.M, w.N, w.K, args.batch)[1]
-        launches_per_step = (1 + (1 if pa or pb else 0) + (1 if tail > 0 else 0)) if packs else 3 * args.batch
-        other_launches = ((["the operand layout pass"] if pa or pb else []) +
-                          (["the last-rows kernel"] if tail > 0 else [])) if packs else \
-            [f"{2 * args.batch} 3xTF32 split passes ({args.batch} entries, one product launch each)"]
+        launches_per_step, other_launches = call_launches(
+            sg, cfg, w.M, w.N, w.K, lda_g, ldb_g, ldc_g, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), num_sms,
+            args.config, args.op_a, args.op_b, args.alpha, args.beta, sa, sb, sc, args.batch)
         total_bytes = 4 * args.batch * (sa + sb + sc)
         flops = args.batch * product_flops(w.M, w.N, w.K)
 

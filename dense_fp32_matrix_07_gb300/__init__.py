@@ -32,7 +32,8 @@ SGEMM_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("sgemm", "sgemm_ex", "sgemm_check_status", "sgemm_error_string",
             "sgemm_num_configs", "sgemm_config_name", "sgemm_plan", "sgemm_noalloc",
             "sgemm_test_withhold_copy", "sgemm_test_schedule", "sgemm_plan_row_tail",
-            "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex", "sgemm_general_plan")
+            "sgemm_test_fail_next_allocs", "sgemm_general", "sgemm_general_ex", "sgemm_general_plan",
+            "sgemm_general_plan_launches")
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +84,8 @@ def load(rebuild: bool = False):
                                                _i64, _i64, _i64, _i64, ctypes.c_float, _i64, _i64, _i64,
                                                ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
                                                ctypes.c_int, _pi, _pi, _pi]
+            lib.sgemm_general_plan_launches.restype = ctypes.c_int
+            lib.sgemm_general_plan_launches.argtypes = lib.sgemm_general_plan.argtypes[:19] + [_pi]
             lib.sgemm_check_status.restype = ctypes.c_int
             lib.sgemm_check_status.argtypes = [_vp]
             lib.sgemm_error_string.restype = ctypes.c_char_p
@@ -215,6 +218,16 @@ def sgemm_general_plan(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b,
                                    stride_c, batch, a_addr, b_addr, c_addr, num_sms, config,
                                    ctypes.byref(cfg), ctypes.byref(pa), ctypes.byref(pb))
     return rc, cfg.value, pa.value, pb.value
+
+
+def sgemm_general_plan_launches(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b, beta, ldc, stride_c,
+                                batch, a_addr, b_addr, c_addr, num_sms, config=-1):
+    """Host-only: (status, kernels of this library that sgemm_general_ex() would launch)."""
+    n = ctypes.c_int(-1)
+    rc = load().sgemm_general_plan_launches(op_a, op_b, M, N, K, alpha, lda, stride_a, ldb, stride_b, beta, ldc,
+                                            stride_c, batch, a_addr, b_addr, c_addr, num_sms, config,
+                                            ctypes.byref(n))
+    return rc, n.value
 
 
 def config_ids() -> dict:

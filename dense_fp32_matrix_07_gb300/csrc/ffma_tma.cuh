@@ -593,7 +593,7 @@ size_t workspace_bytes(const Schedule &s)
 template <class Cfg>
 size_t counter_bytes(const GemmArgs &g)
 {
-    if (g.workspace == nullptr) return 0;
+    if (g.workspace_bytes == 0) return 0;
     const Schedule s = make_schedule<Cfg>(g, true);
     return g.workspace_bytes >= workspace_bytes<Cfg>(s) ? schedule_counter_bytes(s, Cfg::CONSUMERS) : 0;
 }

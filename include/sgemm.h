@@ -35,14 +35,15 @@
  * memory pool on `stream` and returned on `stream`; it is never exposed.
  * Asynchrony: calls return after enqueueing work on `stream`; results are
  * ready when the stream's work completes. An FFMA call enqueues at most
- * three kernels: one layout pass for the operands that need it (it also
- * zeroes the stream-K arrival counters), the product, which for K a
- * multiple of its slab depth may start while that pass finishes
- * (programmatic dependent launch; its threads wait for the pass before they
- * touch memory), and the kernel of the last rows that
- * sgemm_plan_row_tail() describes. Without a layout pass, a memset of the
- * arrival counters precedes the product. A 3xTF32 call enqueues two split
- * passes and the product per batch entry. No call synchronises the host.
+ * three kernels: one layout pass for the operands that need it, which also
+ * zeroes the arrival counters of the stream-K tail and of the last-rows
+ * kernel (with no operand to lay out but counters to zero it runs as one
+ * block); the product, which for K a multiple of its slab depth may start
+ * while that pass finishes (programmatic dependent launch; its threads wait
+ * for the pass before they touch memory); and the kernel of the last rows
+ * that sgemm_plan_row_tail() describes. A 3xTF32 call enqueues two split
+ * passes and the product per batch entry (and a memset of its stream-K
+ * counters). No call synchronises the host.
  * Graph capture: sgemm(), sgemm_ex(), sgemm_general() and sgemm_general_ex()
  * may be captured into a CUDA graph once one call has run on the device
  * (the first call sets the device up); a replay computes the product of
@@ -215,6 +216,28 @@ int sgemm_general_plan(int op_a, int op_b, int64_t M, int64_t N, int64_t K, floa
                        uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
                        int num_sms, int config,
                        int *out_config, int *out_pack_a, int *out_pack_b);
+
+/*
+ * sgemm_general_plan_launches — host only: how many of this library's
+ * kernels sgemm_general_ex() enqueues for these arguments (sgemm_ex() is the
+ * plain form: op 0, alpha 1, beta 0, batch 1). An FFMA configuration runs
+ * the product, the layout pass when an operand goes through scratch or
+ * arrival counters must be zeroed (stream-K tail, split last-rows kernel),
+ * and the last-rows kernel (sgemm_plan_row_tail()); a 3xTF32 configuration
+ * two split passes and the product per batch entry; K == 0 or alpha == 0 one
+ * scaling kernel unless beta == 1. Memory copies and memsets are not
+ * counted.
+ *
+ * Arguments as sgemm_general_plan(); out_launches (not NULL) receives the
+ * count (0 when the call enqueues nothing). Returns SGEMM_OK, or the code
+ * sgemm_general_ex() would return, or SGEMM_ERR_INVALID_VALUE for a NULL
+ * out_launches or num_sms <= 0.
+ */
+int sgemm_general_plan_launches(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                                int64_t lda, int64_t stride_a, int64_t ldb, int64_t stride_b,
+                                float beta, int64_t ldc, int64_t stride_c, int64_t batch,
+                                uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+                                int num_sms, int config, int *out_launches);
 
 /*
  * sgemm_check_status — waits for `stream`, then reads and clears the current

@@ -202,3 +202,30 @@ def test_row_tail_only_on_tma_ffma_configurations():
     assert sg.sgemm_plan_row_tail(cfg, 4097, 3001, 2049, 65536) == (0, 0)
     assert sg.sgemm_plan_row_tail(-1, 4097, 3001, 2049)[0] == sg.SGEMM_ERR_INVALID_VALUE
     assert sg.sgemm_plan_row_tail(cfg, -1, 3001, 2049)[0] == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_general_plan_launches_counts_the_calls_kernels():
+    """Host-only launch count of a call: the product, the layout pass (for an
+    operand that goes through scratch, or for arrival counters to zero), the
+    last-rows kernel; 3xTF32: two splits and the product per entry; only a
+    scaling kernel when K == 0 or alpha == 0 (none when beta == 1)."""
+    P = sg.sgemm_general_plan_launches
+
+    def plain(M, N, K, lda, ldb, ldc, config=-1):
+        return P(0, 0, M, N, K, 1.0, lda, 0, ldb, 0, 0.0, ldc, 0, 1, 0, 0, 0, 152, config)
+
+    assert plain(4096, 4096, 4096, 4096, 4096, 4096) == (0, 2)     # A transposed, product
+    assert plain(4097, 3001, 2049, 2049, 3001, 3001) == (0, 3)     # pass for A and B, product, last row
+    assert plain(1024, 1024, 1024, 1024, 1024, 1024) == (0, 2)     # counters zeroed, product
+    assert plain(1536, 1536, 1536, 1536, 1536, 1536) == (0, 1)     # whole tiles, aligned: product only
+    assert plain(256, 256, 256, 256, 256, 256) == (0, 1)           # the ladder kernel
+    dp = sg.config_ids()["ffma2_128x256_k32_s4_dp"]
+    assert plain(129, 2048, 1024, 1024, 2051, 2048, dp) == (0, 3)  # pass for B, product, last row
+    tf = sg.config_ids()["tf32x3_pair_128x256_k16_s4"]
+    assert P(0, 0, 512, 512, 512, 1.0, 512, 512 * 512, 512, 512 * 512, 0.0, 512, 512 * 512, 3,
+             0, 0, 0, 152, tf) == (0, 9)
+    assert P(0, 0, 10, 10, 0, 1.0, 1, 0, 10, 0, 0.5, 10, 0, 1, 0, 0, 0, 152) == (0, 1)
+    assert P(0, 0, 10, 10, 0, 1.0, 1, 0, 10, 0, 1.0, 10, 0, 1, 0, 0, 0, 152) == (0, 0)
+    assert P(0, 0, -1, 10, 10, 1.0, 10, 0, 10, 0, 0.0, 10, 0, 1, 0, 0, 0, 152)[0] == sg.SGEMM_ERR_INVALID_VALUE
+    assert sg.load().sgemm_general_plan_launches(0, 0, 10, 10, 10, 1.0, 10, 0, 10, 0, 0.0, 10, 0, 1,
+                                                 0, 0, 0, 152, -1, None) == sg.SGEMM_ERR_INVALID_VALUE
