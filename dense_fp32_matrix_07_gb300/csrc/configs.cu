@@ -27,6 +27,7 @@ const ConfigInfo kConfigTable[kNumConfigs] = {
     {"tf32x3_pair_128x256_k16_s4_dp", kKernTf32x3_pair, kSchedDataParallel, true, false, 128, 256},
     {"ffma2_128x256_k32_s4_ka", kKernFfma2_128x256k32s4ka, kSchedAuto, true, true, 128, 256, true},
     {"ffma2_128x128_k32_s4_ka", kKernFfma2_128x128k32s4ka, kSchedAuto, true, true, 128, 128, true},
+    {"small_32x32_k256", kKernSmall32, kSchedDataParallel, false, false, 32, 32},
 };
 
 bool config_supports(int cfg, const ProblemShape &p)
@@ -46,13 +47,17 @@ bool config_supports(int cfg, const ProblemShape &p)
 int select_config(const ProblemShape &p)
 {
     if (!config_supports(kCfgFfma2_128x128, p)) return kCfgTiledSimple;
-    // Tiny products (up to about 400^3, short K) finish sooner in the pages'
-    // register-tiled kernel (2 x 2 outputs per thread, padded 32 x 32 shared
-    // tiles): no tensor-map set-up, and its small tiles spread over many SMs.
-    // Measured back to back: 256^3 10.3 us (the simple 16 x 16 kernel the
-    // same, 128 x 64 TMA tiles 15.9 us), 320^3 12.4 us (14.6, 18.5), 384^3
-    // 16.4 us (22.5, 17.0); at 512^3 the TMA kernel leads, 18.5 us.
-    if ((double)p.M * (double)p.N * (double)p.K <= 67108864.0 && p.K <= 1024) return kCfgLadderRegisterTiled2x2;
+    // Small products (up to about 400^3, a C of at most 2^19 entries, K up to
+    // 512) finish sooner in the small-product kernel: 32 x 32 tiles over many
+    // SMs, each CTA's K panel loaded at once, no tensor-map set-up. Same-box
+    // A/B with the L2 flushed, against the pages' register-tiled kernel that
+    // had these shapes before and the TMA configuration: 256^3 10.7 us
+    // (16.9, 17.9 for 128 x 64 tiles), 384^3 14.8 (23.3), 512 x 512 x 256 14.6
+    // (22.1, 17.9), 64^3 8.5 (10.3 TMA); the TMA tiles lead once C grows
+    // (1024 x 1024 x 64: 17.9 against 10.2 us), once K does (256 x 256 x
+    // 1024: 25.2 against 22.0 us) and from 448^3 on (20.9 against 20.0 us).
+    const double mn = (double)p.M * (double)p.N;
+    if (mn * (double)p.K <= 67108864.0 && p.K <= 512 && mn <= 524288.0) return kCfgSmall32;
     // The widest thread tile (8x16) when there are enough 128x256 tiles to
     // give every SM one; 128x128 down to a third of that (at 1024^3, 64
     // tiles: 49.2 us against 51.2 us for 128x64), 128x64 (two CTAs per SM)
@@ -124,6 +129,7 @@ cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 {
     const int kernel = kConfigTable[cfg].kernel;
     if (kernel == kKernTiledSimple) return launch_tiled_simple(g, stream);
+    if (kernel == kKernSmall32) return launch_small(g, stream);
     if (kernel >= kKernTf32x3_128x256) {
         GemmArgs a = g;
         if (a.sched != kSchedDataParallel) a.sched = kConfigTable[cfg].sched;
@@ -137,8 +143,9 @@ cudaError_t launch_config(int cfg, const GemmArgs &g, cudaStream_t stream)
 
 cudaError_t configs_prepare_device()
 {
-    const cudaError_t e = prepare_ffma_tma();
-    return e != cudaSuccess ? e : prepare_tf32x3();
+    cudaError_t e = prepare_ffma_tma();
+    if (e == cudaSuccess) e = prepare_tf32x3();
+    return e != cudaSuccess ? e : prepare_small();
 }
 
 }  // namespace sgemm_gb300

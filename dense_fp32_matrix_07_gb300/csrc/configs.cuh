@@ -34,7 +34,9 @@ enum KernelId : int {
     // Tensor cores (kernels_tf32x3.cu): 3xTF32 split, tcgen05.mma into TMEM.
     kKernTf32x3_128x256,
     kKernTf32x3_128x128,
-    kKernTf32x3_pair            // 128x256 per CTA, clusters of 2 along M multicasting B
+    kKernTf32x3_pair,           // 128x256 per CTA, clusters of 2 along M multicasting B
+    // Small products (kernels_small.cu): 32x32 tiles, the K panel loaded at once.
+    kKernSmall32
 };
 
 // Configurations = kernel instance + schedule policy.
@@ -62,6 +64,7 @@ enum ConfigId : int {
     kCfgTf32x3_pair_dp,
     kCfgFfma2_128x256_ka,
     kCfgFfma2_128x128_ka,
+    kCfgSmall32,
     kNumConfigs
 };
 
@@ -112,6 +115,10 @@ cudaError_t prepare_ffma_tma_ktail();
 // g.behind_pack is set.
 cudaError_t launch_ffma_tma_dep(int kernel, const GemmArgs &g, cudaStream_t stream);
 cudaError_t prepare_ffma_tma_dep();
+
+// The small-product kernel (kernels_small.cu), plain form only, any layout.
+cudaError_t launch_small(const GemmArgs &g, cudaStream_t stream);
+cudaError_t prepare_small();
 
 // Launcher of the ladder kernels (kernels_ladder.cu), by KernelId.
 cudaError_t launch_ladder(int kernel, const GemmArgs &g, cudaStream_t stream);

@@ -269,8 +269,8 @@ static int plan_call(const Call &c, int num_sms, int *out_cfg, bool *out_pa, boo
     const bool plain = c.op_a == 0 && c.op_b == 0 && c.alpha == 1.0f && c.beta == 0.0f && c.batch == 1;
     const ProblemShape p{c.M, c.N, c.K, c.lda, c.ldb, c.ldc, a, b, cp, num_sms};
     int cfg = c.config < 0 ? select_config(p) : c.config;
-    // The automatic choice for tiny products is a plain-form-only kernel of
-    // the pages' ladder; the general form takes the smallest TMA tiles instead.
+    // The automatic choice for small products is a plain-form-only kernel;
+    // the general form takes the smallest TMA tiles instead.
     if (c.config < 0 && !plain && !kConfigTable[cfg].uses_tma) cfg = kCfgFfma2_128x64;
     // An A stored transposed (K x M) is what the k-major configurations read
     // in place, with no transposing pack: take them whenever their row-major

@@ -89,15 +89,14 @@ def test_plan_packs_only_misaligned_operands():
     assert rc == 0 and (pa, pb) == (1, 0)
     rc, cfg, pa, pb = sg.sgemm_plan(1024, 1024, 1024, 1024, 1024, 1024, 0, 8, 12, 148)
     assert rc == 0 and (pa, pb) == (0, 1)
-    # The register-tiled kernel of the pages' ladder (tiny products) reads any
-    # layout in place.
+    # The small-product kernel reads any layout in place.
     rc, cfg, pa, pb = sg.sgemm_plan(256, 256, 256, 256, 256, 256, 4, 8, 12, 148)
-    assert rc == 0 and sg.sgemm_config_name(cfg) == "ladder_register_tiled_2x2" and (pa, pb) == (0, 0)
+    assert rc == 0 and sg.sgemm_config_name(cfg) == "small_32x32_k256" and (pa, pb) == (0, 0)
 
 
 @pytest.mark.parametrize("n,name", [
-    (256, "ladder_register_tiled_2x2"), # tiny: no TMA set-up, small tiles over many SMs
-    (384, "ladder_register_tiled_2x2"),
+    (256, "small_32x32_k256"),          # small: no TMA set-up, 32x32 tiles, each K panel loaded at once
+    (384, "small_32x32_k256"),
     (512, "ffma2_128x64_k32_s4"),       # 16 tiles of 128x128: the smallest TMA tiles
     (1024, "ffma2_128x128_k32_s4"),     # 64 tiles of 128x128 (>= a third of the SMs)
     (2048, "ffma2_128x128_k32_s4_ka"),  # 128 tiles of 128x256 < 148 SMs; N >= 2048: A k-major
@@ -109,6 +108,9 @@ def test_plan_tile_size_follows_the_problem(n, name):
 
 
 @pytest.mark.parametrize("M,N,K,name", [
+    (512, 512, 256, "small_32x32_k256"),            # C of 2^18, K 256: the small-product kernel
+    (1024, 1024, 64, "ffma2_128x128_k32_s4"),       # C of 2^20: TMA tiles, although M*N*K = 2^26
+    (256, 256, 1024, "ffma2_128x64_k32_s4"),        # K 1024: TMA tiles (stream-K), M*N*K = 2^26
     (2048, 2048, 512, "ffma2_128x128_k32_s4"),      # M*N*K = 2.1e9: the transpose pass would not pay
     (4096, 4096, 256, "ffma2_128x256_k32_s4"),      # 4.3e9: the same on 128x256 tiles
     (1536, 2048, 2048, "ffma2_128x128_k32_s4_ka"),  # 6.4e9 and N >= 2048: A k-major
@@ -218,7 +220,7 @@ def test_general_plan_launches_counts_the_calls_kernels():
     assert plain(4097, 3001, 2049, 2049, 3001, 3001) == (0, 3)     # pass for A and B, product, last row
     assert plain(1024, 1024, 1024, 1024, 1024, 1024) == (0, 2)     # counters zeroed, product
     assert plain(1536, 1536, 1536, 1536, 1536, 1536) == (0, 1)     # whole tiles, aligned: product only
-    assert plain(256, 256, 256, 256, 256, 256) == (0, 1)           # the ladder kernel
+    assert plain(256, 256, 256, 256, 256, 256) == (0, 1)           # the small-product kernel
     dp = sg.config_ids()["ffma2_128x256_k32_s4_dp"]
     assert plain(129, 2048, 1024, 1024, 2051, 2048, dp) == (0, 3)  # pass for B, product, last row
     tf = sg.config_ids()["tf32x3_pair_128x256_k16_s4"]
