@@ -173,8 +173,9 @@ int sgemm_ex(int64_t M, int64_t N, int64_t K,
  * persistent launch (their tiles are one schedule), on the 3xTF32 ones each
  * entry is split and multiplied in turn. Status codes as sgemm();
  * SGEMM_ERR_UNSUPPORTED if
- * a forced configuration cannot run the general form (the simple and the
- * kernel-ladder configurations run only the plain form).
+ * a forced configuration cannot run the general form (the simple, the
+ * kernel-ladder and the small-product configurations run only the plain
+ * form; the automatic choice gives the general form TMA tiles instead).
  */
 int sgemm_general(int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
                   const float *A, int64_t lda, int64_t stride_a,
