@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(256) pack_transpose_batched_kernel(const PackJ
 
 // Both operands' layout passes of one product in one launch: blocks
 // [0, a.blocks) run job a, the next b.blocks run job b, and one more block
-// zeroes `zero_words` words (the product's stream-K arrival counters). Every
+// zeroes `zero_words` words (the arrival counters of the product's stream-K
+// region and of the row-tail kernel; with no job, that block is the whole
+// launch). Every
 // block first allows a kernel queued behind this one with programmatic
 // serialization (the product, which waits for this grid's completion before
 // it reads anything) to start taking SMs as this grid's last blocks run.
