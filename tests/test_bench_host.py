@@ -162,3 +162,29 @@ def test_unknown_extra_workload_is_rejected_before_any_device_work():
 
 def test_cpu_model_is_named():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_gpu_launches_follow_the_library_plan():
+    """bench.py counts the library's launches per step from the library's own
+    host-only plan: the product, the layout pass (operands to lay out or
+    counters to zero), the last-rows kernel; 3xTF32 two splits and the
+    product per entry."""
+    import dense_fp32_matrix_07_gb300 as sg
+
+    def plain(M, N, K, lda, ldb, ldc, config=-1):
+        _, cfg, _, _ = sg.sgemm_general_plan(0, 0, M, N, K, 1.0, lda, 0, ldb, 0, 0.0, ldc, 0, 1, 0, 0, 0, 152,
+                                             config)
+        return bench.call_launches(sg, cfg, M, N, K, lda, ldb, ldc, 0, 0, 0, 152, config)
+
+    n, other = plain(4096, 4096, 4096, 4096, 4096, 4096)
+    assert n == 2 and other == ["the layout pass (operand copies, counter zeroing)"]
+    n, other = plain(4097, 3001, 2049, 2049, 3001, 3001)
+    assert n == 3 and other[-1] == "the last-rows kernel"
+    assert plain(1536, 1536, 1536, 1536, 1536, 1536) == (1, [])
+    assert plain(256, 256, 256, 256, 256, 256) == (1, [])
+    tf = sg.config_ids()["tf32x3_pair_128x256_k16_s4"]
+    _, cfg, _, _ = sg.sgemm_general_plan(0, 0, 512, 512, 512, 1.0, 512, 512 * 512, 512, 512 * 512, 0.0, 512,
+                                         512 * 512, 2, 0, 0, 0, 152, tf)
+    n, other = bench.call_launches(sg, cfg, 512, 512, 512, 512, 512, 512, 0, 0, 0, 152, tf, sa=512 * 512,
+                                   sb=512 * 512, sc=512 * 512, batch=2)
+    assert n == 6 and "3xTF32 split passes" in other[0]
