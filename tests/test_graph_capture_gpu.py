@@ -1,5 +1,6 @@
 """sgemm calls captured in a CUDA graph and replayed: the library's work on a
-stream (pool scratch, the stream-K flag memset, cooperative and cluster
+stream (pool scratch, the layout pass and the product queued behind it with
+programmatic serialization, the row-tail kernel behind the product, cluster
 launches) must be capturable, and a replay must compute the product of the
 inputs present at replay time. Checked against the oracle."""
 
@@ -15,11 +16,7 @@ pytestmark = pytest.mark.gpu
 IDS = sg.config_ids()
 
 
-@pytest.mark.parametrize("config_name", [None, "ffma2_128x256_k32_s4_sk", "ffma2_128x256_k32_s4_ka",
-                                         "ffma2_128x128_k32_s4", "tf32x3_pair_128x256_k16_s4"])
-def test_captured_products_replay_correctly(cuda_device, oracle, config_name):
-    M, N, K = 700, 900, 515          # several tiles, ragged edges, stream-K tail on the auto path
-    config = -1 if config_name is None else IDS[config_name]
+def _capture_and_replay(oracle, M, N, K, config):
     dA = torch.empty((M, K), device="cuda")
     dB = torch.empty((K, N), device="cuda")
     dC = torch.full((M, N), float("nan"), device="cuda")
@@ -55,6 +52,22 @@ def test_captured_products_replay_correctly(cuda_device, oracle, config_name):
             assert np.array_equal(C, Cref.astype(np.float32).astype(np.float64)), seed
         else:
             assert np.all(np.abs(C - Cref) <= 1e-4 * S), seed
+
+
+@pytest.mark.parametrize("config_name", [None, "ffma2_128x256_k32_s4_sk", "ffma2_128x256_k32_s4_ka",
+                                         "ffma2_128x128_k32_s4", "tf32x3_pair_128x256_k16_s4"])
+def test_captured_products_replay_correctly(cuda_device, oracle, config_name):
+    # Several tiles, ragged edges (K = 515 also trims the last slab), the
+    # layout pass of the k-major configuration, the stream-K tail.
+    _capture_and_replay(oracle, 700, 900, 515, -1 if config_name is None else IDS[config_name])
+
+
+@pytest.mark.parametrize("M,N,K", [(385, 1024, 2048), (1153, 2048, 2560), (200, 300, 150)])
+def test_captured_launch_chains_replay_correctly(cuda_device, oracle, M, N, K):
+    # The automatic choice: the one-block counter zeroing, the product behind
+    # it and the row-tail kernel behind the product (385 rows; 1153 rows with
+    # the k-major layout pass first), and the small-product kernel.
+    _capture_and_replay(oracle, M, N, K, -1)
 
 
 def test_captured_general_form_with_packing(cuda_device, oracle):
